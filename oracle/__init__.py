@@ -1,0 +1,164 @@
+"""CPU oracle for the multi-scale deformable attention core -- TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline /
+reference leg may import this package.  The shipped library never does, and this
+package imports nothing from it: the oracle is plain C (``msda_oracle.c``) evaluated
+in double precision, loaded here through ctypes.
+
+Every function takes numpy arrays in the layouts of ``workloads`` and returns float64
+arrays.  Inputs are widened to float64 exactly (fp32 and bf16 values are exact in
+double), so the oracle and the CUDA path see the same input values.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Dict, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "msda_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libmsda_oracle.so")
+_lib = None
+
+_I64 = ctypes.c_int64
+_DP = ctypes.POINTER(ctypes.c_double)
+_LP = ctypes.POINTER(ctypes.c_int64)
+
+
+def compile_source(src: str, out_path: str) -> str:
+    """Compile an oracle source file with gcc (IEEE double, no FMA contraction)."""
+    tmp = out_path + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                    "-shared", "-fPIC", "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def build(force: bool = False) -> str:
+    """Compile ``msda_oracle.c`` into ``_build/libmsda_oracle.so`` when stale."""
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        os.makedirs(_BUILD_DIR, exist_ok=True)
+        compile_source(_SRC, _LIB_PATH)
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    """Bind another build of the oracle source (used by the mutation tests)."""
+    return _bind(path)
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    fwd_args = [_I64] * 7 + [_LP, _LP, _DP, _DP, _DP, _DP]
+    bwd_args = [_I64] * 7 + [_LP, _LP, _DP, _DP, _DP, _DP, _DP, _DP, _DP]
+    for name in ("oracle_msda2d_forward", "oracle_msda3d_forward"):
+        getattr(lib, name).argtypes = fwd_args
+        getattr(lib, name).restype = ctypes.c_int
+    for name in ("oracle_msda2d_backward", "oracle_msda3d_backward"):
+        getattr(lib, name).argtypes = bwd_args
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _bind(build())
+    return _lib
+
+
+def _d(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+def _ptr(a: np.ndarray, t):
+    return a.ctypes.data_as(t)
+
+
+def _dims(value: np.ndarray, loc: np.ndarray, shapes: np.ndarray, nd: int):
+    B, Nin, M, D = value.shape
+    if loc.ndim != 6 or loc.shape[-1] != nd:
+        raise ValueError(f"sampling_locations must be [B,Nq,M,L,P,{nd}], got {loc.shape}")
+    _, Nq, M2, L, P, _ = loc.shape
+    if M2 != M or loc.shape[0] != B or shapes.shape != (L, nd):
+        raise ValueError("inconsistent shapes")
+    return B, Nin, Nq, M, D, L, P
+
+
+def forward(nd: int, value, spatial_shapes, level_start_index, sampling_locations,
+            attention_weights, lib=None) -> np.ndarray:
+    """out[B, Nq, M*D] in float64.  ``lib`` selects another build of the oracle."""
+    v, loc, a = _d(value), _d(sampling_locations), _d(attention_weights)
+    sh, ls = _i(spatial_shapes), _i(level_start_index)
+    B, Nin, Nq, M, D, L, P = _dims(v, loc, sh, nd)
+    out = np.zeros((B, Nq, M * D), dtype=np.float64)
+    lib = lib or _load()
+    fn = lib.oracle_msda2d_forward if nd == 2 else lib.oracle_msda3d_forward
+    rc = fn(B, Nin, Nq, M, D, L, P, _ptr(sh, _LP), _ptr(ls, _LP), _ptr(v, _DP),
+            _ptr(loc, _DP), _ptr(a, _DP), _ptr(out, _DP))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out
+
+
+def backward(nd: int, value, spatial_shapes, level_start_index, sampling_locations,
+             attention_weights, grad_out, lib=None) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """(grad_value, grad_sampling_locations, grad_attention_weights) in float64."""
+    v, loc, a = _d(value), _d(sampling_locations), _d(attention_weights)
+    g = _d(grad_out)
+    sh, ls = _i(spatial_shapes), _i(level_start_index)
+    B, Nin, Nq, M, D, L, P = _dims(v, loc, sh, nd)
+    gv = np.zeros_like(v)
+    gl = np.zeros_like(loc)
+    ga = np.zeros_like(a)
+    lib = lib or _load()
+    fn = lib.oracle_msda2d_backward if nd == 2 else lib.oracle_msda3d_backward
+    rc = fn(B, Nin, Nq, M, D, L, P, _ptr(sh, _LP), _ptr(ls, _LP), _ptr(v, _DP),
+            _ptr(loc, _DP), _ptr(a, _DP), _ptr(g, _DP), _ptr(gv, _DP), _ptr(gl, _DP),
+            _ptr(ga, _DP))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return gv, gl, ga
+
+
+def msda2d_forward(value, spatial_shapes, level_start_index, sampling_locations,
+                   attention_weights):
+    return forward(2, value, spatial_shapes, level_start_index, sampling_locations,
+                   attention_weights)
+
+
+def msda3d_forward(value, spatial_shapes, level_start_index, sampling_locations,
+                   attention_weights):
+    return forward(3, value, spatial_shapes, level_start_index, sampling_locations,
+                   attention_weights)
+
+
+def msda2d_backward(value, spatial_shapes, level_start_index, sampling_locations,
+                    attention_weights, grad_out):
+    return backward(2, value, spatial_shapes, level_start_index, sampling_locations,
+                    attention_weights, grad_out)
+
+
+def msda3d_backward(value, spatial_shapes, level_start_index, sampling_locations,
+                    attention_weights, grad_out):
+    return backward(3, value, spatial_shapes, level_start_index, sampling_locations,
+                    attention_weights, grad_out)
+
+
+def run_inputs(nd: int, inp: Dict[str, np.ndarray], backward_pass: bool = False, lib=None):
+    """Convenience: run the oracle on a dict from ``workloads.make_inputs``."""
+    args = (inp["value"], inp["spatial_shapes"], inp["level_start_index"],
+            inp["sampling_locations"], inp["attention_weights"])
+    if backward_pass:
+        return backward(nd, *args, inp["grad_out"], lib=lib)
+    return forward(nd, *args, lib=lib)
