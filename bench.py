@@ -1,0 +1,565 @@
+#!/usr/bin/env python3
+"""Benchmark of the multi-scale deformable attention core on B300 (libmsda).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the hot path over one batch of synthetic input: by default the
+forward of the encoder-shaped workload (B=2, 4-level pyramid 100x150..13x19, Nq=Nin=19947,
+M=8, D=32, P=4, fp32), i.e. the coordinate transform, corner gather, interpolation /
+weighted sum and store.  Other workloads: tiny2d, decoder2d, volume3d (forward) and
+encoder2d_bwd (zero-fill + backward).
+
+Prints ONE JSON line (rank 0).  `value` is samples (B*Nq*M*L*P) per second over all ranks,
+timed on the device with CUDA events on the launching stream over exactly K steps
+(barrier + synchronize on both sides, max over ranks).  L2 is kept cold by rotating over
+input sets whose total size is more than twice the L2 capacity.  `e2e` is the same metric
+through the public binding with pinned host buffers, host->device copies of the inputs and
+the device->host copy of the output inside the timed region.  `cpu_baseline` times the CPU
+oracle (test infrastructure) on the host, single-threaded.
+
+Under torchrun (N > 1) every rank runs its own batch of the workload (weak scaling; no
+collective on the data path; NCCL is used only for the barrier and the max of the times).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "sampled points/s (B·Nq·M·L·P per s) and achieved HBM GB/s vs ~8 TB/s peak"
+UNIT = "samples/s"
+FALLBACK_HBM_GBS = 6400.0
+L2_BYTES = 126 * 2 ** 20
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SRC_DIR = os.path.join(ROOT, "scale_deformable_attention_msda3d_b300", "csrc")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA / C++ sources of libmsda (identifies the measured kernels)."""
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(KERNEL_SRC_DIR)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(f.encode())
+            h.update(open(os.path.join(KERNEL_SRC_DIR, f), "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    src = kernel_source_hash()
+    if not os.path.isdir(PROFILE_DIR):
+        return None
+    for f in sorted(os.listdir(PROFILE_DIR)):
+        if not f.endswith((".md", ".txt")):
+            continue
+        text = open(os.path.join(PROFILE_DIR, f)).read()
+        m_w = re.search(r"^bench_workload:\s*(\S+)", text, re.M)
+        m_h = re.search(r"^kernel_source_sha256:\s*([0-9a-f]{64})", text, re.M)
+        m_t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        if m_w and m_h and m_t and m_w.group(1) == workload and m_h.group(1) == src:
+            return float(m_t.group(1))
+    return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return float(d["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def unique_value_rows(w: workloads.Workload, inp) -> int:
+    """Distinct (batch, value row, head) rows touched by at least one corner that lies
+    inside its level: the value bytes a perfect cache would read once."""
+    loc = inp["sampling_locations"].astype(np.float64)
+    B, Nq, M, L, P, nd = loc.shape
+    starts = inp["level_start_index"]
+    ids = []
+    b_idx = np.arange(B).reshape(B, 1, 1, 1)
+    m_idx = np.arange(M).reshape(1, 1, M, 1)
+    for l in range(L):
+        shape = [int(s) for s in inp["spatial_shapes"][l]]
+        ext = shape[::-1]                                   # (W, H[, Z])
+        pix = loc[:, :, :, l] * np.array(ext, dtype=np.float64) - 0.5   # [B,Nq,M,P,nd]
+        ok_s = np.all((pix > -1) & (pix < np.array(ext)), axis=-1)
+        i0 = np.floor(np.where(np.isfinite(pix), pix, -5)).astype(np.int64)
+        for c in range(2 ** nd):
+            d = np.array([(c >> k) & 1 for k in range(nd)])
+            idx = i0 + d
+            inside = ok_s & np.all((idx >= 0) & (idx < np.array(ext)), axis=-1)
+            if nd == 2:
+                row = idx[..., 1] * ext[0] + idx[..., 0]
+            else:
+                row = (idx[..., 2] * ext[1] + idx[..., 1]) * ext[0] + idx[..., 0]
+            gid = ((b_idx * w.Nin + starts[l] + row) * M + m_idx)
+            ids.append(gid[inside])
+    return int(np.unique(np.concatenate(ids)).size)
+
+
+def algorithmic_bytes(w: workloads.Workload, inp) -> dict:
+    esize = 2 if w.dtype == "bf16" else 4
+    row = w.D * esize
+    uniq = unique_value_rows(w, inp) * row
+    loc_b = inp["sampling_locations"].nbytes
+    attn_b = inp["attention_weights"].nbytes
+    out_b = w.B * w.Nq * w.M * w.D * esize
+    whole_value = w.B * w.Nin * w.M * row
+    if not w.backward:
+        total = uniq + loc_b + attn_b + out_b
+        parts = dict(unique_value=uniq, locations=loc_b, weights=attn_b, out=out_b)
+    else:
+        gv = w.B * w.Nin * w.M * w.D * 4
+        total = uniq + loc_b + attn_b + out_b + gv + loc_b + attn_b + gv   # + zero-fill
+        parts = dict(unique_value=uniq, locations=loc_b, weights=attn_b, grad_out=out_b,
+                     grad_value=gv, grad_locations=loc_b, grad_weights=attn_b,
+                     grad_value_zero_fill=gv)
+    parts["whole_value_tensor"] = whole_value
+    return dict(total=int(total), parts=parts)
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while the GPU works."""
+
+    REASONS = {
+        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
+        "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
+        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+        "display_clock_setting": 0x100,
+    }
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self.period = period_s
+        self._stop = threading.Event()
+        self._t = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nvml = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # NVML missing: report no clocks rather than guess
+            self._nvml = None
+            self.error = str(e)
+
+    def sample_once(self):
+        if self._nvml is None:
+            return
+        n = self._nvml
+        try:
+            self.samples.append(n.nvmlDeviceGetClockInfo(self._h, n.NVML_CLOCK_SM))
+            r = n.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+            for name, bit in self.REASONS.items():
+                if r & bit:
+                    self.reasons.add(name)
+        except Exception:
+            pass
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.sample_once()
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t is not None:
+            self._t.join()
+
+    def summary(self):
+        if self._nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.error}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
+                "reasons": sorted(self.reasons - {"gpu_idle"})}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+
+def dist_setup(want_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif want_gpus > 1:
+        print(f"--gpus {want_gpus} needs torchrun (one process per GPU); running 1 rank",
+              file=sys.stderr)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def all_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def all_sum(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- our arm
+
+
+def to_device(inp, w, dev):
+    import torch
+    if w.dtype == "bf16":
+        value = torch.from_numpy(inp["value_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        value = torch.from_numpy(inp["value"]).to(dev)
+    d = dict(value=value,
+             loc=torch.from_numpy(inp["sampling_locations"]).to(dev),
+             attn=torch.from_numpy(inp["attention_weights"]).to(dev))
+    if w.backward:
+        if w.dtype == "bf16":
+            d["grad_out"] = torch.from_numpy(inp["grad_out_bits"].view(np.int16)).to(dev).view(
+                torch.bfloat16)
+        else:
+            d["grad_out"] = torch.from_numpy(inp["grad_out"]).to(dev)
+    return d
+
+
+def make_step(msda, w, inp, bufs, stream):
+    """Returns step(i): one pass of the hot path on input set i % len(bufs)."""
+    shapes, starts = inp["spatial_shapes"], inp["level_start_index"]
+    if not w.backward:
+        fn = msda.msda2d_forward if w.ndim == 2 else msda.msda3d_forward
+
+        def step(i):
+            b = bufs[i % len(bufs)]
+            fn(b["value"], shapes, starts, b["loc"], b["attn"], out=b["out"], stream=stream)
+        return step, 1
+    fn = msda.msda2d_backward if w.ndim == 2 else msda.msda3d_backward
+
+    def step(i):
+        b = bufs[i % len(bufs)]
+        fn(b["value"], shapes, starts, b["loc"], b["attn"], b["grad_out"],
+           grad_value=b["gv"], grad_sampling_locations=b["gl"],
+           grad_attention_weights=b["ga"], stream=stream)
+    return step, 2
+
+
+def cpu_baseline(w, inp, budget_s: float = 10.0):
+    """The oracle as it stands (single-threaded C, double precision) on the full workload,
+    repeated until ~budget_s of CPU time; samples per second."""
+    import oracle
+    oracle.build()
+    args = [np.ascontiguousarray(inp[k], dtype=np.float64) for k in
+            ("value", "sampling_locations", "attention_weights")]
+    shapes, starts = inp["spatial_shapes"], inp["level_start_index"]
+    g = np.ascontiguousarray(inp["grad_out"], dtype=np.float64) if w.backward else None
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        if w.backward:
+            oracle.backward(w.ndim, args[0], shapes, starts, args[1], args[2], g)
+        else:
+            oracle.forward(w.ndim, args[0], shapes, starts, args[1], args[2])
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": w.samples * runs / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{runs} full pass(es) of the {w.name} workload "
+                      f"({w.samples} samples each), {el:.1f} s, 1 thread, fp64"}
+
+
+def run_ours(args):
+    import torch
+    import scale_deformable_attention_msda3d_b300 as msda
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    msda.load()
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(w, seed=w.seed + rank)
+    base = to_device(inp, w, dev)
+    esize = 2 if w.dtype == "bf16" else 4
+    set_bytes = sum(t.numel() * t.element_size() for t in base.values())
+    set_bytes += w.B * w.Nq * w.M * w.D * esize
+    if w.backward:
+        set_bytes += base["value"].numel() * 4 + base["loc"].numel() * 4 + base["attn"].numel() * 4
+    n_sets = max(2, int(np.ceil(2 * L2_BYTES / set_bytes)) + 1)
+    bufs = []
+    for i in range(n_sets):
+        b = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
+        b["out"] = torch.empty((w.B, w.Nq, w.M * w.D), dtype=b["value"].dtype, device=dev)
+        if w.backward:
+            b["gv"] = torch.empty(b["value"].shape, dtype=torch.float32, device=dev)
+            b["gl"] = torch.empty_like(b["loc"])
+            b["ga"] = torch.empty_like(b["attn"])
+        bufs.append(b)
+    stream = torch.cuda.Stream(dev)
+    step, launches_per_step = make_step(msda, w, inp, bufs, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with clocks:
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                step(i)
+        ev1.record(stream)
+        clocks.sample_once()
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    t_rank = ev0.elapsed_time(ev1) / 1e3                      # seconds, this rank
+    t_max = all_max(t_rank, world)
+    samples_all = all_sum(float(w.samples), world) * args.steps
+    value = samples_all / t_max
+    ms_per_step = t_max * 1e3 / args.steps
+
+    # end to end through the public binding, host buffers, copies inside the timed region
+    e2e = run_e2e(msda, w, inp, dev, args, world) if not args.no_e2e else None
+
+    if rank != 0:
+        barrier(world)
+        return None
+    ab = algorithmic_bytes(w, inp)
+    peak, peak_src = measured_peaks()
+    per_launch_s = t_rank / args.steps
+    achieved = ab["total"] / per_launch_s / 1e9
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Nin": w.Nin, "Nq": w.Nq, "M": w.M,
+                   "D": w.D, "L": w.L, "P": w.P, "levels": [list(s) for s in w.shapes],
+                   "ndim": w.ndim, "pass": "backward" if w.backward else "forward",
+                   "samples_per_step_per_gpu": w.samples,
+                   "l2": f"cold: {n_sets} rotating input sets of {set_bytes / 1e6:.1f} MB "
+                         f"(> 2x L2) between steps",
+                   "parallelism": f"weak: {world} rank(s), one batch each, no collective"},
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.4 TB/s",
+                     "algorithmic_bytes_per_launch": ab["total"],
+                     "bytes_breakdown": ab["parts"],
+                     "kernel": "msda fwd" if not w.backward else "zero-fill + msda bwd"},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clocks.summary(),
+        "kernel_source_sha256": kernel_source_hash(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, budget_s=args.cpu_budget)
+    barrier(world)
+    return line
+
+
+def run_e2e(msda, w, inp, dev, args, world):
+    import torch
+    pin = {}
+    if w.dtype == "bf16":
+        pin["value"] = torch.from_numpy(inp["value_bits"].view(np.int16)).view(
+            torch.bfloat16).pin_memory()
+    else:
+        pin["value"] = torch.from_numpy(inp["value"]).pin_memory()
+    pin["loc"] = torch.from_numpy(inp["sampling_locations"]).pin_memory()
+    pin["attn"] = torch.from_numpy(inp["attention_weights"]).pin_memory()
+    if w.backward:
+        pin["grad_out"] = (torch.from_numpy(inp["grad_out_bits"].view(np.int16)).view(
+            torch.bfloat16) if w.dtype == "bf16" else torch.from_numpy(inp["grad_out"])
+        ).pin_memory()
+    d = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pin.items()}
+    stream = torch.cuda.Stream(dev)
+    shapes, starts = inp["spatial_shapes"], inp["level_start_index"]
+    if not w.backward:
+        out_h = torch.empty((w.B, w.Nq, w.M * w.D), dtype=d["value"].dtype).pin_memory()
+        out_d = torch.empty(out_h.shape, dtype=out_h.dtype, device=dev)
+        fn = msda.msda2d_forward if w.ndim == 2 else msda.msda3d_forward
+        outs_h = [out_h]
+    else:
+        fn = msda.msda2d_backward if w.ndim == 2 else msda.msda3d_backward
+        outs_h = [torch.empty(d["value"].shape, dtype=torch.float32).pin_memory(),
+                  torch.empty(pin["loc"].shape, dtype=torch.float32).pin_memory(),
+                  torch.empty(pin["attn"].shape, dtype=torch.float32).pin_memory()]
+        outs_d = [torch.empty(o.shape, dtype=o.dtype, device=dev) for o in outs_h]
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs_h)
+
+    def one():
+        with torch.cuda.stream(stream):
+            for k in pin:
+                d[k].copy_(pin[k], non_blocking=True)
+            if not w.backward:
+                fn(d["value"], shapes, starts, d["loc"], d["attn"], out=out_d, stream=stream)
+                out_h.copy_(out_d, non_blocking=True)
+            else:
+                fn(d["value"], shapes, starts, d["loc"], d["attn"], d["grad_out"],
+                   grad_value=outs_d[0], grad_sampling_locations=outs_d[1],
+                   grad_attention_weights=outs_d[2], stream=stream)
+                for o_h, o_d in zip(outs_h, outs_d):
+                    o_h.copy_(o_d, non_blocking=True)
+
+    steps = max(3, min(args.steps, args.e2e_steps))
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    ev0.record(stream)
+    for _ in range(steps):
+        one()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    t = max(ev0.elapsed_time(ev1) / 1e3, 0.0)
+    t_max = all_max(max(t, wall), world)
+    samples_all = all_sum(float(w.samples), world) * steps
+    return {"value": samples_all / t_max, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": t_max * 1e3 / steps,
+            "path": "pinned host -> device copies, libmsda call, device -> pinned host copy, "
+                    "one stream"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+
+def run_reference(args):
+    """The CPU oracle as it stands, timed on the host cores on this arm's workload and
+    metric; each step is a bounded sample (a contiguous block of queries of batch 0)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(w)
+    per_q = w.M * w.L * w.P                                  # samples per query
+    shapes, starts = inp["spatial_shapes"], inp["level_start_index"]
+    value = np.ascontiguousarray(inp["value"][:1], dtype=np.float64)
+    loc = np.ascontiguousarray(inp["sampling_locations"][:1], dtype=np.float64)
+    attn = np.ascontiguousarray(inp["attention_weights"][:1], dtype=np.float64)
+    g = (np.ascontiguousarray(inp["grad_out"][:1], dtype=np.float64) if w.backward else None)
+
+    def run(q0, q1):
+        sl = slice(q0, q1)
+        if w.backward:
+            oracle.backward(w.ndim, value, shapes, starts, loc[:, sl], attn[:, sl], g[:, sl])
+        else:
+            oracle.forward(w.ndim, value, shapes, starts, loc[:, sl], attn[:, sl])
+
+    # calibrate: size one step to ~min(0.5 s, 90 s / (K + W))
+    nq = min(w.Nq, 256)
+    t0 = time.perf_counter()
+    run(0, nq)
+    rate_q = nq / max(time.perf_counter() - t0, 1e-6)
+    budget = min(0.5, 90.0 / max(1, args.steps + args.warmup))
+    nq = int(max(1, min(w.Nq, rate_q * budget)))
+    for i in range(args.warmup):
+        q0 = (i * nq) % max(1, w.Nq - nq + 1)
+        run(q0, q0 + nq)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        q0 = (i * nq) % max(1, w.Nq - nq + 1)
+        run(q0, q0 + nq)
+    el = time.perf_counter() - t0
+    v = nq * per_q * args.steps / el
+    sample = (f"each step: queries [q0, q0+{nq}) of batch 0 of the {w.name} workload "
+              f"({nq * per_q} samples), all heads/levels/points; 1 thread, fp64 oracle")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Nin": w.Nin, "Nq": w.Nq, "M": w.M,
+                       "D": w.D, "L": w.L, "P": w.P,
+                       "pass": "backward" if w.backward else "forward"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=workloads.names(), default="encoder2d")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for the cpu_baseline leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,144 @@
+/*
+ * libmsda -- multi-scale deformable attention core for NVIDIA B300 (sm_103a).
+ *
+ * The operation ("Deformable Attention Module", Code with Papers: the DeformAttn equation
+ * and the paragraph under it; "3D Attention That Knows Where to Look": the per-query
+ * recipe, the multi-scale paragraph and "What changes from 2D to 3D"):
+ *
+ *   out[b, q, m*D + d] = sum_{l < L} sum_{p < P}  A[b,q,m,l,p] * x_l(loc[b,q,m,l,p])[m, d]
+ *
+ * where x_l(.) samples level l of the per-head value map bilinearly (2D: the 4 pixels
+ * around the location) or trilinearly (3D: the 8 corners of the surrounding voxel cell).
+ * The attention weights A are used as given (callers normalise them over the L x P
+ * samples of each query and head; the library never renormalises).  The projections
+ * W_m / W'_m of the full module are not part of this core.
+ *
+ * Sampling convention (the pages do not fix one; this is the library's definition):
+ *   pixel coordinate  x = loc_x * W_l - 0.5,  y = loc_y * H_l - 0.5  [, z = loc_z * Z_l - 0.5]
+ *   (grid_sample with align_corners = false).  Corners outside level l contribute zero
+ *   and receive no gradient (zero padding); a sample with a non-finite coordinate
+ *   contributes zero and gets zero gradients.  At an integer coordinate the cell chosen
+ *   by floor() defines the (right-hand) location gradient.
+ *
+ * Layouts (row-major, last index fastest; all device memory unless marked host):
+ *   value                [B, Nin, M, D]          value dtype (fp32 or bf16)
+ *   spatial_shapes       host int64 [L][2] = (H, W)   or  [L][3] = (Z, H, W)
+ *   level_start_index    host int64 [L], must equal the exclusive prefix sum of the
+ *                        level sizes; the sizes must add up to Nin.  Pixel (h, w) of
+ *                        level l is value row level_start_index[l] + h*W + w; voxel
+ *                        (z, h, w) is row level_start_index[l] + (z*H + h)*W + w.
+ *   sampling_locations   [B, Nq, M, L, P, 2|3]   fp32, normalised (x, y[, z]):
+ *                        component 0 runs along W, 1 along H, 2 along Z.
+ *   attention_weights    [B, Nq, M, L, P]        fp32
+ *   out / grad_out       [B, Nq, M*D]            value dtype
+ *   grad_value           [B, Nin, M, D]          fp32 (always)
+ *   grad_sampling_locations   like sampling_locations, fp32
+ *   grad_attention_weights    like attention_weights,  fp32
+ *
+ * Ownership and execution: the caller owns every buffer; these calls allocate no memory
+ * (no cudaMalloc / cudaFree).  Work is enqueued on `stream` (0 = legacy default stream)
+ * and the call returns without synchronising.  Outputs are overwritten, never
+ * accumulated into.  The backward zero-fills grad_value itself, on `stream`.
+ *
+ * Errors: arguments are validated on the host BEFORE anything is enqueued; a failed
+ * check returns MSDA_ERR_INVALID_ARG or MSDA_ERR_UNSUPPORTED with nothing enqueued.  A
+ * launch failure returns MSDA_ERR_CUDA.  Faults during execution surface at the caller's
+ * next synchronisation, as for any CUDA work.  msda_last_error() gives a message for the
+ * last non-OK status returned on the calling thread.
+ *
+ * Limits: 1 <= L <= MSDA_MAX_LEVELS, 1 <= P <= MSDA_MAX_POINTS, Nin < 2^31, every level
+ * extent in [1, 2^24); D * sizeof(value dtype) must be 16, 32, 64, 128, 256 or 512 bytes
+ * (fp32: D in {4, 8, 16, 32, 64, 128}; bf16: D in {8, 16, 32, 64, 128, 256}); every
+ * pointer must be 16-byte aligned.  B == 0 or Nq == 0 is a valid empty call (the
+ * backward then still zero-fills grad_value).
+ */
+#ifndef MSDA_H_
+#define MSDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t, without including CUDA headers. */
+typedef struct CUstream_st *msda_stream_t;
+
+#define MSDA_MAX_LEVELS 16
+#define MSDA_MAX_POINTS 32
+
+typedef enum {
+    MSDA_OK = 0,
+    MSDA_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent shapes, misalignment */
+    MSDA_ERR_UNSUPPORTED = 2, /* valid but outside the compiled set (D, L, P, dtype)      */
+    MSDA_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed                      */
+    MSDA_ERR_INTERNAL = 4
+} msda_status;
+
+typedef enum { MSDA_F32 = 0, MSDA_BF16 = 1 } msda_dtype;
+
+typedef struct {
+    int64_t B;        /* batch                                   */
+    int64_t Nin;      /* value rows per batch (all levels)        */
+    int64_t Nq;       /* queries per batch                        */
+    int32_t M;        /* heads                                    */
+    int32_t D;        /* channels per head                        */
+    int32_t L;        /* pyramid levels                           */
+    int32_t P;        /* sampling points per level                */
+    int32_t value_dtype; /* msda_dtype of value, out and grad_out */
+} msda_dims;
+
+/*
+ * 2D forward: out = sum over levels and points of A times the bilinear sample.
+ * Defined by the DeformAttn equation ("Deformable Attention Module") with the
+ * multi-scale sum of "3D Attention That Knows Where to Look".
+ */
+msda_status msda2d_forward(const msda_dims *dims, const void *value,
+                           const int64_t *spatial_shapes, const int64_t *level_start_index,
+                           const float *sampling_locations, const float *attention_weights,
+                           void *out, msda_stream_t stream);
+
+/*
+ * 2D backward: given grad_out = dLoss/dout, writes dLoss/dvalue (fp32), dLoss/dlocations
+ * and dLoss/dweights ("3D Attention That Knows Where to Look": gradients flow back into
+ * both the offsets and the weights; the value gradient is the transpose of the gather).
+ * grad_value is zero-filled on `stream` first, then accumulated with atomics, so its
+ * summation order (and last bits) may vary between runs.
+ */
+msda_status msda2d_backward(const msda_dims *dims, const void *value,
+                            const int64_t *spatial_shapes, const int64_t *level_start_index,
+                            const float *sampling_locations, const float *attention_weights,
+                            const void *grad_out, float *grad_value,
+                            float *grad_sampling_locations, float *grad_attention_weights,
+                            msda_stream_t stream);
+
+/*
+ * 3D forward: as msda2d_forward with trilinear sampling over the 8 corners of the voxel
+ * cell ("3D Attention That Knows Where to Look", "What changes from 2D to 3D"):
+ * spatial_shapes is [L][3] = (Z, H, W) and locations are (x, y, z).
+ */
+msda_status msda3d_forward(const msda_dims *dims, const void *value,
+                           const int64_t *spatial_shapes, const int64_t *level_start_index,
+                           const float *sampling_locations, const float *attention_weights,
+                           void *out, msda_stream_t stream);
+
+/* 3D backward: as msda2d_backward, trilinear, three location components. */
+msda_status msda3d_backward(const msda_dims *dims, const void *value,
+                            const int64_t *spatial_shapes, const int64_t *level_start_index,
+                            const float *sampling_locations, const float *attention_weights,
+                            const void *grad_out, float *grad_value,
+                            float *grad_sampling_locations, float *grad_attention_weights,
+                            msda_stream_t stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none).  The string
+ * is owned by the library and stays valid until the next call on the same thread. */
+const char *msda_last_error(void);
+
+/* Version of this interface (major * 10000 + minor * 100 + patch). */
+int32_t msda_abi_version(void);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* MSDA_H_ */

@@ -1,0 +1,272 @@
+"""ctypes binding of libmsda (include/msda.h): argument marshalling only.
+
+Every computation runs in the CUDA kernels of libmsda.so; this module only turns torch
+tensors into pointers, sizes and a stream handle, calls the C ABI and raises on a non-OK
+status.  There is no CPU fallback: if the library cannot be built or loaded, the first
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence, Tuple, Union
+
+import numpy as np
+
+from . import build as _build
+
+MSDA_OK, MSDA_ERR_INVALID_ARG, MSDA_ERR_UNSUPPORTED, MSDA_ERR_CUDA, MSDA_ERR_INTERNAL = range(5)
+MSDA_F32, MSDA_BF16 = 0, 1
+MSDA_MAX_LEVELS = 16
+MSDA_MAX_POINTS = 32
+
+STATUS_NAMES = {0: "MSDA_OK", 1: "MSDA_ERR_INVALID_ARG", 2: "MSDA_ERR_UNSUPPORTED",
+                3: "MSDA_ERR_CUDA", 4: "MSDA_ERR_INTERNAL"}
+
+# Every symbol include/msda.h declares.
+EXPORTS = ("msda2d_forward", "msda2d_backward", "msda3d_forward", "msda3d_backward",
+           "msda_last_error", "msda_abi_version")
+
+
+class MsdaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class msda_dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("Nin", ctypes.c_int64), ("Nq", ctypes.c_int64),
+                ("M", ctypes.c_int32), ("D", ctypes.c_int32), ("L", ctypes.c_int32),
+                ("P", ctypes.c_int32), ("value_dtype", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+_VP = ctypes.c_void_p
+_I64P = ctypes.POINTER(ctypes.c_int64)
+_DIMS_P = ctypes.POINTER(msda_dims)
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: Optional[str] = None):
+    """Load libmsda.so (building it in-tree first when missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        if path is None:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libmsda not found at {path}")
+        lib = ctypes.CDLL(path)
+        fwd = [_DIMS_P, _VP, _I64P, _I64P, _VP, _VP, _VP, _VP]
+        bwd = [_DIMS_P, _VP, _I64P, _I64P, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
+        for name in ("msda2d_forward", "msda3d_forward"):
+            getattr(lib, name).argtypes = fwd
+            getattr(lib, name).restype = ctypes.c_int
+        for name in ("msda2d_backward", "msda3d_backward"):
+            getattr(lib, name).argtypes = bwd
+            getattr(lib, name).restype = ctypes.c_int
+        lib.msda_last_error.argtypes = []
+        lib.msda_last_error.restype = ctypes.c_char_p
+        lib.msda_abi_version.argtypes = []
+        lib.msda_abi_version.restype = ctypes.c_int32
+        if path == _build.LIB:
+            _lib = lib
+        return lib
+
+
+def _check(lib, status: int) -> None:
+    if status != MSDA_OK:
+        raise MsdaError(status, lib.msda_last_error().decode(errors="replace"))
+
+
+# ----------------------------------------------------------------------------- raw layer
+# Plain pointers (ints), host metadata arrays and a cudaStream_t (int), as in the header.
+
+
+def _host_i64(a) -> np.ndarray:
+    if hasattr(a, "detach"):  # torch tensor
+        if a.is_cuda:
+            raise ValueError("spatial_shapes / level_start_index are host arrays; pass CPU "
+                             "tensors or numpy arrays")
+        a = a.detach().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int64))
+
+
+def make_dims(B, Nin, Nq, M, D, L, P, value_dtype) -> msda_dims:
+    return msda_dims(int(B), int(Nin), int(Nq), int(M), int(D), int(L), int(P),
+                     int(value_dtype))
+
+
+def forward_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes, level_start_index,
+                sampling_locations: int, attention_weights: int, out: int, stream: int = 0,
+                lib=None) -> int:
+    """Call msda{2,3}d_forward with raw device pointers; returns the status (no raise)."""
+    lib = lib or load()
+    sh, ls = _host_i64(spatial_shapes), _host_i64(level_start_index)
+    fn = lib.msda2d_forward if ndim == 2 else lib.msda3d_forward
+    return fn(ctypes.byref(dims), _VP(value), sh.ctypes.data_as(_I64P),
+              ls.ctypes.data_as(_I64P), _VP(sampling_locations), _VP(attention_weights),
+              _VP(out), _VP(stream))
+
+
+def backward_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes, level_start_index,
+                 sampling_locations: int, attention_weights: int, grad_out: int,
+                 grad_value: int, grad_sampling_locations: int, grad_attention_weights: int,
+                 stream: int = 0, lib=None) -> int:
+    lib = lib or load()
+    sh, ls = _host_i64(spatial_shapes), _host_i64(level_start_index)
+    fn = lib.msda2d_backward if ndim == 2 else lib.msda3d_backward
+    return fn(ctypes.byref(dims), _VP(value), sh.ctypes.data_as(_I64P),
+              ls.ctypes.data_as(_I64P), _VP(sampling_locations), _VP(attention_weights),
+              _VP(grad_out), _VP(grad_value), _VP(grad_sampling_locations),
+              _VP(grad_attention_weights), _VP(stream))
+
+
+# ----------------------------------------------------------------------------- torch layer
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return MSDA_F32
+    if t.dtype == torch.bfloat16:
+        return MSDA_BF16
+    raise MsdaError(MSDA_ERR_UNSUPPORTED, f"value dtype {t.dtype} (supported: float32, bfloat16)")
+
+
+def _require(t, name: str, dtype=None):
+    if not t.is_cuda:
+        raise MsdaError(MSDA_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise MsdaError(MSDA_ERR_INVALID_ARG, f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise MsdaError(MSDA_ERR_INVALID_ARG, f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _stream_handle(stream, device) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dims_from(value, sampling_locations, ndim: int) -> msda_dims:
+    if value.dim() != 4:
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "value must be [B, Nin, M, D]")
+    if sampling_locations.dim() != 6 or sampling_locations.shape[-1] != ndim:
+        raise MsdaError(MSDA_ERR_INVALID_ARG,
+                        f"sampling_locations must be [B, Nq, M, L, P, {ndim}]")
+    B, Nin, M, D = value.shape
+    B2, Nq, M2, L, P, _ = sampling_locations.shape
+    if B2 != B or M2 != M:
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "value and sampling_locations disagree on B or M")
+    return make_dims(B, Nin, Nq, M, D, L, P, _dtype_code(value))
+
+
+def _forward(ndim, value, spatial_shapes, level_start_index, sampling_locations,
+             attention_weights, out=None, stream=None):
+    torch = _torch()
+    dims = _dims_from(value, sampling_locations, ndim)
+    _require(value, "value")
+    _require(sampling_locations, "sampling_locations", torch.float32)
+    _require(attention_weights, "attention_weights", torch.float32)
+    if tuple(attention_weights.shape) != tuple(sampling_locations.shape[:-1]):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "attention_weights must be [B, Nq, M, L, P]")
+    if out is None:
+        out = torch.empty((dims.B, dims.Nq, dims.M * dims.D), dtype=value.dtype,
+                          device=value.device)
+    _require(out, "out", value.dtype)
+    if tuple(out.shape) != (dims.B, dims.Nq, dims.M * dims.D):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "out must be [B, Nq, M*D]")
+    lib = load()
+    st = forward_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
+                     sampling_locations.data_ptr(), attention_weights.data_ptr(),
+                     out.data_ptr(), _stream_handle(stream, value.device), lib=lib)
+    _check(lib, st)
+    return out
+
+
+def _backward(ndim, value, spatial_shapes, level_start_index, sampling_locations,
+              attention_weights, grad_out, grad_value=None, grad_sampling_locations=None,
+              grad_attention_weights=None, stream=None):
+    torch = _torch()
+    dims = _dims_from(value, sampling_locations, ndim)
+    _require(value, "value")
+    _require(sampling_locations, "sampling_locations", torch.float32)
+    _require(attention_weights, "attention_weights", torch.float32)
+    _require(grad_out, "grad_out", value.dtype)
+    if tuple(grad_out.shape) != (dims.B, dims.Nq, dims.M * dims.D):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "grad_out must be [B, Nq, M*D]")
+    dev = value.device
+    if grad_value is None:
+        grad_value = torch.empty(value.shape, dtype=torch.float32, device=dev)
+    if grad_sampling_locations is None:
+        grad_sampling_locations = torch.empty_like(sampling_locations)
+    if grad_attention_weights is None:
+        grad_attention_weights = torch.empty_like(attention_weights)
+    _require(grad_value, "grad_value", torch.float32)
+    _require(grad_sampling_locations, "grad_sampling_locations", torch.float32)
+    _require(grad_attention_weights, "grad_attention_weights", torch.float32)
+    lib = load()
+    st = backward_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
+                      sampling_locations.data_ptr(), attention_weights.data_ptr(),
+                      grad_out.data_ptr(), grad_value.data_ptr(),
+                      grad_sampling_locations.data_ptr(), grad_attention_weights.data_ptr(),
+                      _stream_handle(stream, dev), lib=lib)
+    _check(lib, st)
+    return grad_value, grad_sampling_locations, grad_attention_weights
+
+
+def msda2d_forward(value, spatial_shapes, level_start_index, sampling_locations,
+                   attention_weights, out=None, stream=None):
+    """2D forward (bilinear).  value [B,Nin,M,D] fp32/bf16 CUDA; spatial_shapes [L,2] and
+    level_start_index [L] on the HOST; sampling_locations [B,Nq,M,L,P,2] and
+    attention_weights [B,Nq,M,L,P] fp32 CUDA.  Returns out [B,Nq,M*D] (value dtype),
+    enqueued on ``stream`` (default: torch's current stream)."""
+    return _forward(2, value, spatial_shapes, level_start_index, sampling_locations,
+                    attention_weights, out, stream)
+
+
+def msda3d_forward(value, spatial_shapes, level_start_index, sampling_locations,
+                   attention_weights, out=None, stream=None):
+    """3D forward (trilinear); spatial_shapes [L,3] = (Z,H,W), locations (x,y,z)."""
+    return _forward(3, value, spatial_shapes, level_start_index, sampling_locations,
+                    attention_weights, out, stream)
+
+
+def msda2d_backward(value, spatial_shapes, level_start_index, sampling_locations,
+                    attention_weights, grad_out, grad_value=None, grad_sampling_locations=None,
+                    grad_attention_weights=None, stream=None):
+    """2D backward.  Returns (grad_value fp32, grad_sampling_locations, grad_attention_weights)."""
+    return _backward(2, value, spatial_shapes, level_start_index, sampling_locations,
+                     attention_weights, grad_out, grad_value, grad_sampling_locations,
+                     grad_attention_weights, stream)
+
+
+def msda3d_backward(value, spatial_shapes, level_start_index, sampling_locations,
+                    attention_weights, grad_out, grad_value=None, grad_sampling_locations=None,
+                    grad_attention_weights=None, stream=None):
+    """3D backward (trilinear)."""
+    return _backward(3, value, spatial_shapes, level_start_index, sampling_locations,
+                     attention_weights, grad_out, grad_value, grad_sampling_locations,
+                     grad_attention_weights, stream)
+
+
+def msda_last_error() -> str:
+    lib = load()
+    return lib.msda_last_error().decode(errors="replace")
+
+
+def msda_abi_version() -> int:
+    return int(load().msda_abi_version())

@@ -1,0 +1,62 @@
+"""torch.autograd wrapper around the libmsda forward / backward calls (marshalling only)."""
+from __future__ import annotations
+
+import numpy as np
+
+from . import _binding
+
+
+def _import_torch():
+    import torch
+    return torch
+
+
+class _Fn:
+    """Lazily built autograd.Function so that importing the package does not need torch."""
+    cls = None
+
+    @classmethod
+    def get(cls):
+        if cls.cls is None:
+            torch = _import_torch()
+
+            class MSDeformAttn(torch.autograd.Function):
+                @staticmethod
+                def forward(ctx, value, spatial_shapes, level_start_index,
+                            sampling_locations, attention_weights):
+                    ndim = sampling_locations.shape[-1]
+                    shapes = np.asarray(spatial_shapes, dtype=np.int64)
+                    starts = np.asarray(level_start_index, dtype=np.int64)
+                    fwd = _binding.msda2d_forward if ndim == 2 else _binding.msda3d_forward
+                    out = fwd(value, shapes, starts, sampling_locations, attention_weights)
+                    ctx.save_for_backward(value, sampling_locations, attention_weights)
+                    ctx.meta = (ndim, shapes, starts)
+                    return out
+
+                @staticmethod
+                def backward(ctx, grad_out):
+                    value, loc, attn = ctx.saved_tensors
+                    ndim, shapes, starts = ctx.meta
+                    bwd = _binding.msda2d_backward if ndim == 2 else _binding.msda3d_backward
+                    gv, gl, ga = bwd(value, shapes, starts, loc, attn, grad_out.contiguous())
+                    return gv.to(value.dtype), None, None, gl, ga
+
+            cls.cls = MSDeformAttn
+        return cls.cls
+
+
+class MSDeformAttnFunction:
+    """``MSDeformAttnFunction.apply(value, spatial_shapes, level_start_index, loc, attn)``."""
+
+    @staticmethod
+    def apply(value, spatial_shapes, level_start_index, sampling_locations, attention_weights):
+        return _Fn.get().apply(value, spatial_shapes, level_start_index, sampling_locations,
+                               attention_weights)
+
+
+def ms_deform_attn(value, spatial_shapes, level_start_index, sampling_locations,
+                   attention_weights):
+    """Differentiable multi-scale deformable attention core (2D or 3D by the last dim of
+    ``sampling_locations``).  ``spatial_shapes`` / ``level_start_index`` are host arrays."""
+    return MSDeformAttnFunction.apply(value, spatial_shapes, level_start_index,
+                                      sampling_locations, attention_weights)

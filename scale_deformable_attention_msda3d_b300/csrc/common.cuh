@@ -1,0 +1,94 @@
+// Device-side building blocks shared by the libmsda kernels (sm_103a).
+//
+// Value rows are moved in 16-byte pieces: a "lane group" of G consecutive lanes owns one
+// (batch, query, head) work item, and lane k of the group owns bytes [16k, 16k+16) of
+// every D-channel value row the item touches (4 fp32 or 8 bf16 channels).  One warp-wide
+// 16-byte load therefore fetches 32/G complete rows, each a contiguous, fully used span.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "msda_internal.h"
+
+namespace msda {
+
+// Channels held by one lane (16 bytes of the value dtype).
+template <int DT> struct Vec;
+template <> struct Vec<kF32> { static constexpr int N = 4; static constexpr int ESIZE = 4; };
+template <> struct Vec<kBF16> { static constexpr int N = 8; static constexpr int ESIZE = 2; };
+
+// Read-only 16-byte load through the non-coherent (texture/L1) path.
+__device__ __forceinline__ uint4 ldg16(const void *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// 16 bytes of fp32 / bf16 channels -> fp32 registers.
+__device__ __forceinline__ void unpack(const uint4 &u, float (&v)[4]) {
+    v[0] = __uint_as_float(u.x);
+    v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z);
+    v[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void unpack(const uint4 &u, float (&v)[8]) {
+    // a bf16 is the high half of the fp32 with the same value
+    v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xffff0000u);
+    v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xffff0000u);
+    v[4] = __uint_as_float(u.z << 16); v[5] = __uint_as_float(u.z & 0xffff0000u);
+    v[6] = __uint_as_float(u.w << 16); v[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+// fp32 registers -> 16 bytes of the value dtype (bf16: round to nearest even, once).
+__device__ __forceinline__ uint4 pack(const float (&v)[4]) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                      __float_as_uint(v[3]));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint4 pack(const float (&v)[8]) {
+    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                      pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
+// Normalised location -> pixel coordinate on one axis: x = loc * extent - 0.5
+// (align_corners = false).  Returns the cell index floor(x) and the fraction x - floor(x).
+//
+// The product loc * extent is rounded once to fp32 and its exact rounding error is
+// recovered with an FMA and folded into the fraction, so the fraction is accurate to about
+// 1e-7 of a pixel relative to the exact double-precision coordinate, independent of the
+// extent.  (Rounding x itself to fp32 would cost up to ~8e-6 px at extent 150.)
+// Intrinsics with explicit rounding keep the compiler from contracting the product and
+// the subtraction into one FMA, which would lose the error term.
+//
+// A coordinate that is not finite or lies at or beyond -1 / the extent is reported as
+// invalid (every corner outside); the outputs are then i0 = -2, frac = 0, so all corner
+// tests fail and no weight is NaN.
+__device__ __forceinline__ bool pixel_coord(float loc, float extent, int &i0, float &frac) {
+    const float prod = __fmul_rn(loc, extent);
+    const float err = __fmaf_rn(loc, extent, -prod);
+    const float x = __fsub_rn(prod, 0.5f);
+    const bool ok = (x > -1.0f) && (x < extent);
+    const float xf = floorf(x);
+    frac = ok ? __fadd_rn(__fsub_rn(x, xf), err) : 0.0f;
+    i0 = ok ? static_cast<int>(xf) : -2;
+    return ok;
+}
+
+// Vector reduction of 4 fp32 values into global memory (no return value).
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
+    atomicAdd(reinterpret_cast<float4 *>(addr), make_float4(a, b, c, d));
+}
+
+// Sum over the G lanes of a lane group (G a power of two dividing 32); every lane of the
+// warp must call it with the same G.
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace msda

@@ -1,0 +1,231 @@
+// C ABI of libmsda: host-side validation, parameter packing and dispatch.
+// Nothing is enqueued unless every check passes; no memory is allocated.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "../../include/msda.h"
+#include "msda_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+msda_status fail(msda_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t *r) { return !__builtin_mul_overflow(a, b, r); }
+
+bool misaligned(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; }
+
+// Validates sizes and level metadata and fills the kernel parameters.
+// `need_query_ptrs` is true when there is per-query work (B * Nq > 0).
+msda_status build_params(const msda_dims *d, int ndim, const int64_t *shapes,
+                         const int64_t *level_start, msda::Params *p, int *G) {
+    if (!d) return fail(MSDA_ERR_INVALID_ARG, "dims is NULL");
+    if (d->value_dtype != MSDA_F32 && d->value_dtype != MSDA_BF16)
+        return fail(MSDA_ERR_INVALID_ARG, "value_dtype %d is not MSDA_F32 or MSDA_BF16",
+                    d->value_dtype);
+    if (d->B < 0 || d->Nq < 0)
+        return fail(MSDA_ERR_INVALID_ARG, "B (%lld) and Nq (%lld) must be >= 0",
+                    (long long)d->B, (long long)d->Nq);
+    if (d->Nin < 1 || d->M < 1 || d->D < 1 || d->L < 1 || d->P < 1)
+        return fail(MSDA_ERR_INVALID_ARG, "Nin, M, D, L, P must be >= 1 (got %lld %d %d %d %d)",
+                    (long long)d->Nin, d->M, d->D, d->L, d->P);
+    if (d->L > MSDA_MAX_LEVELS)
+        return fail(MSDA_ERR_UNSUPPORTED, "L = %d exceeds MSDA_MAX_LEVELS = %d", d->L,
+                    MSDA_MAX_LEVELS);
+    if (d->P > MSDA_MAX_POINTS)
+        return fail(MSDA_ERR_UNSUPPORTED, "P = %d exceeds MSDA_MAX_POINTS = %d", d->P,
+                    MSDA_MAX_POINTS);
+    if (d->Nin > INT32_MAX)
+        return fail(MSDA_ERR_UNSUPPORTED, "Nin = %lld must be below 2^31", (long long)d->Nin);
+    if (!shapes || !level_start)
+        return fail(MSDA_ERR_INVALID_ARG, "spatial_shapes / level_start_index is NULL");
+
+    const int esize = d->value_dtype == MSDA_F32 ? 4 : 2;
+    const int64_t dbytes = int64_t(d->D) * esize;
+    if (dbytes % 16 != 0 || dbytes > 512 || ((dbytes / 16) & (dbytes / 16 - 1)) != 0)
+        return fail(MSDA_ERR_UNSUPPORTED,
+                    "D * sizeof(dtype) = %lld bytes; supported: 16, 32, 64, 128, 256, 512",
+                    (long long)dbytes);
+    *G = int(dbytes / 16);
+
+    int64_t total = 0;
+    for (int l = 0; l < d->L; ++l) {
+        int64_t size = 1;
+        for (int k = 0; k < ndim; ++k) {
+            const int64_t e = shapes[l * ndim + k];
+            if (e < 1 || e >= (int64_t(1) << 24))
+                return fail(MSDA_ERR_INVALID_ARG,
+                            "spatial_shapes[%d][%d] = %lld must be in [1, 2^24)", l, k,
+                            (long long)e);
+            if (!mul_ok(size, e, &size) || size > INT32_MAX)
+                return fail(MSDA_ERR_INVALID_ARG, "level %d has too many pixels", l);
+        }
+        if (level_start[l] != total)
+            return fail(MSDA_ERR_INVALID_ARG,
+                        "level_start_index[%d] = %lld, expected the prefix sum %lld", l,
+                        (long long)level_start[l], (long long)total);
+        total += size;
+        if (total > d->Nin) break;
+    }
+    if (total != d->Nin)
+        return fail(MSDA_ERR_INVALID_ARG, "level sizes add up to %lld, Nin is %lld",
+                    (long long)total, (long long)d->Nin);
+
+    int64_t t;
+    if (!mul_ok(d->B, d->Nin, &t) || !mul_ok(t, d->M, &t) || !mul_ok(t, d->D, &t) ||
+        !mul_ok(t, 4, &t))
+        return fail(MSDA_ERR_INVALID_ARG, "B * Nin * M * D overflows");
+    int64_t items;
+    if (!mul_ok(d->B, d->Nq, &items) || !mul_ok(items, d->M, &items) ||
+        !mul_ok(items, int64_t(d->L) * d->P * 3 * 4, &t) || !mul_ok(items, 32, &t))
+        return fail(MSDA_ERR_INVALID_ARG, "B * Nq * M * L * P overflows");
+
+    std::memset(p, 0, sizeof(*p));
+    p->B = d->B;
+    p->Nin = d->Nin;
+    p->Nq = d->Nq;
+    p->M = d->M;
+    p->D = d->D;
+    p->L = d->L;
+    p->P = d->P;
+    p->n_items = items;
+    p->row_bytes = int64_t(d->M) * dbytes;
+    for (int l = 0; l < d->L; ++l) {
+        const int64_t *s = shapes + l * ndim;
+        p->W[l] = int(s[ndim - 1]);
+        p->H[l] = int(s[ndim - 2]);
+        p->Z[l] = ndim == 3 ? int(s[0]) : 1;
+        p->fW[l] = float(p->W[l]);
+        p->fH[l] = float(p->H[l]);
+        p->fZ[l] = float(p->Z[l]);
+        p->start[l] = int(level_start[l]);
+    }
+    return MSDA_OK;
+}
+
+msda_status check_ptr(const void *ptr, const char *name) {
+    if (!ptr) return fail(MSDA_ERR_INVALID_ARG, "%s is NULL", name);
+    if (misaligned(ptr)) return fail(MSDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+    return MSDA_OK;
+}
+
+#define MSDA_TRY(expr)                         \
+    do {                                       \
+        const msda_status st_ = (expr);        \
+        if (st_ != MSDA_OK) return st_;        \
+    } while (0)
+
+msda_status cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return MSDA_OK;
+    return fail(MSDA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+msda_status forward_impl(int ndim, const msda_dims *dims, const void *value,
+                         const int64_t *shapes, const int64_t *level_start, const float *loc,
+                         const float *attn, void *out, msda_stream_t stream) {
+    msda::Params p;
+    int G = 0;
+    MSDA_TRY(build_params(dims, ndim, shapes, level_start, &p, &G));
+    if (p.n_items == 0) return MSDA_OK;  // empty batch or no queries: nothing to compute
+    MSDA_TRY(check_ptr(value, "value"));
+    MSDA_TRY(check_ptr(loc, "sampling_locations"));
+    MSDA_TRY(check_ptr(attn, "attention_weights"));
+    MSDA_TRY(check_ptr(out, "out"));
+    p.value = value;
+    p.loc = loc;
+    p.attn = attn;
+    p.out = out;
+    return cuda_status(msda::launch_forward(ndim, dims->value_dtype, G, p,
+                                            reinterpret_cast<cudaStream_t>(stream)),
+                       "forward launch");
+}
+
+msda_status backward_impl(int ndim, const msda_dims *dims, const void *value,
+                          const int64_t *shapes, const int64_t *level_start, const float *loc,
+                          const float *attn, const void *grad_out, float *grad_value,
+                          float *grad_loc, float *grad_attn, msda_stream_t stream) {
+    msda::Params p;
+    int G = 0;
+    MSDA_TRY(build_params(dims, ndim, shapes, level_start, &p, &G));
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dims->B == 0) return MSDA_OK;
+    MSDA_TRY(check_ptr(grad_value, "grad_value"));
+    if (p.n_items > 0) {
+        MSDA_TRY(check_ptr(value, "value"));
+        MSDA_TRY(check_ptr(loc, "sampling_locations"));
+        MSDA_TRY(check_ptr(attn, "attention_weights"));
+        MSDA_TRY(check_ptr(grad_out, "grad_out"));
+        MSDA_TRY(check_ptr(grad_loc, "grad_sampling_locations"));
+        MSDA_TRY(check_ptr(grad_attn, "grad_attention_weights"));
+    }
+    MSDA_TRY(cuda_status(msda::launch_zero_fill(grad_value, p.B * p.Nin * p.M * p.D, s),
+                         "grad_value zero-fill launch"));
+    p.value = value;
+    p.loc = loc;
+    p.attn = attn;
+    p.grad_out = grad_out;
+    p.grad_value = grad_value;
+    p.grad_loc = grad_loc;
+    p.grad_attn = grad_attn;
+    return cuda_status(msda::launch_backward(ndim, dims->value_dtype, G, p, s),
+                       "backward launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+msda_status msda2d_forward(const msda_dims *dims, const void *value,
+                           const int64_t *spatial_shapes, const int64_t *level_start_index,
+                           const float *sampling_locations, const float *attention_weights,
+                           void *out, msda_stream_t stream) {
+    return forward_impl(2, dims, value, spatial_shapes, level_start_index, sampling_locations,
+                        attention_weights, out, stream);
+}
+
+msda_status msda3d_forward(const msda_dims *dims, const void *value,
+                           const int64_t *spatial_shapes, const int64_t *level_start_index,
+                           const float *sampling_locations, const float *attention_weights,
+                           void *out, msda_stream_t stream) {
+    return forward_impl(3, dims, value, spatial_shapes, level_start_index, sampling_locations,
+                        attention_weights, out, stream);
+}
+
+msda_status msda2d_backward(const msda_dims *dims, const void *value,
+                            const int64_t *spatial_shapes, const int64_t *level_start_index,
+                            const float *sampling_locations, const float *attention_weights,
+                            const void *grad_out, float *grad_value,
+                            float *grad_sampling_locations, float *grad_attention_weights,
+                            msda_stream_t stream) {
+    return backward_impl(2, dims, value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_weights, grad_out, grad_value, grad_sampling_locations,
+                         grad_attention_weights, stream);
+}
+
+msda_status msda3d_backward(const msda_dims *dims, const void *value,
+                            const int64_t *spatial_shapes, const int64_t *level_start_index,
+                            const float *sampling_locations, const float *attention_weights,
+                            const void *grad_out, float *grad_value,
+                            float *grad_sampling_locations, float *grad_attention_weights,
+                            msda_stream_t stream) {
+    return backward_impl(3, dims, value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_weights, grad_out, grad_value, grad_sampling_locations,
+                         grad_attention_weights, stream);
+}
+
+const char *msda_last_error(void) { return g_err; }
+
+int32_t msda_abi_version(void) { return 10000; }
+
+}  // extern "C"

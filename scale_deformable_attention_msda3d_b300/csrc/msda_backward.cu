@@ -1,0 +1,254 @@
+// Backward kernels: gradients of sum(grad_out * out) with respect to value, sampling
+// locations and attention weights ("3D Attention That Knows Where to Look": gradients
+// flow back into both the offsets and the weights; interpolation is differentiable).
+//
+// Per sample with weight a, corner weights w_c (without a) and corner rows v_c:
+//   grad_A        = sum_c w_c <g, v_c>
+//   grad_x (px)   = a * sum_c dw_c/dx <g, v_c>,   grad_loc_x = W_l * grad_x   (x = loc*W - 0.5)
+//   grad_value[c] += a * w_c * g                  (corners inside the level only)
+// The lane group recomputes the sample, forms per-lane partial dot products over its 16
+// bytes of channels, reduces grad_A / grad_loc with xor shuffles inside the group, and
+// scatters grad_value with 16-byte vector reductions (red.global.add.v4.f32).
+#include "common.cuh"
+
+namespace msda {
+
+namespace {
+
+__global__ void zero_fill_kernel(float4 *__restrict__ p, long long n4) {
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += stride)
+        p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// grad_value += wgt * g over the N channels a lane owns (N/4 vector reductions).
+template <int N>
+__device__ __forceinline__ void scatter(float *dst, float wgt, const float (&g)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4)
+        red_add_v4(dst + i, wgt * g[i], wgt * g[i + 1], wgt * g[i + 2], wgt * g[i + 3]);
+}
+
+template <int N>
+__device__ __forceinline__ float dot(const uint4 &u, const float (&g)[N]) {
+    float v[N];
+    unpack(u, v);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) s = fmaf(g[i], v[i], s);
+    return s;
+}
+
+template <int DT, int G, int LL, int PP>
+__global__ void __launch_bounds__(256)
+bwd2d_kernel(const __grid_constant__ Params p) {
+    constexpr int N = Vec<DT>::N;
+    const int L = LL > 0 ? LL : p.L;
+    const int P = PP > 0 ? PP : p.P;
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    // whole warps leave together so that the group shuffles below see every lane
+    if ((t - (threadIdx.x & 31)) / G >= p.n_items) return;
+    long long item = t / G;
+    const bool active = item < p.n_items;
+    if (!active) item = p.n_items - 1;  // tail lanes recompute a real item, write nothing
+    const int sub = threadIdx.x & (G - 1);
+    const int m = static_cast<int>(item % p.M);
+    const long long b = item / p.M / p.Nq;
+    const long long rb = p.row_bytes;
+    const long long rowf = static_cast<long long>(p.M) * p.D;  // grad_value row stride (floats)
+    const char *vb = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
+                     static_cast<long long>(m) * (rb / p.M) + sub * 16;
+    float *gvb = p.grad_value + (b * p.Nin) * rowf + static_cast<long long>(m) * p.D + sub * N;
+    float g[N];
+    unpack(ldg16(static_cast<const char *>(p.grad_out) + item * (rb / p.M) + sub * 16), g);
+    const long long s0 = item * L * P;
+    const float2 *lp = reinterpret_cast<const float2 *>(p.loc) + s0;
+
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+        const int W = p.W[l], H = p.H[l];
+        const float fW = p.fW[l], fH = p.fH[l];
+        const char *vl = vb + static_cast<long long>(p.start[l]) * rb;
+        float *gl = gvb + static_cast<long long>(p.start[l]) * rowf;
+#pragma unroll 2
+        for (int k = 0; k < P; ++k) {
+            const long long s = s0 + l * P + k;
+            const float2 xy = __ldg(lp + l * P + k);
+            const float a = __ldg(p.attn + s);
+            int x0, y0;
+            float fx, fy;
+            pixel_coord(xy.x, fW, x0, fx);
+            pixel_coord(xy.y, fH, y0, fy);
+            const bool vx0 = x0 >= 0, vx1 = x0 < W - 1;
+            const bool vy0 = y0 >= 0, vy1 = y0 < H - 1;
+            const bool ok00 = vy0 && vx0, ok01 = vy0 && vx1, ok10 = vy1 && vx0, ok11 = vy1 && vx1;
+            const long long r00 = static_cast<long long>(y0 * W + x0);
+            const char *c00 = vl + r00 * rb;
+            uint4 u00 = make_uint4(0, 0, 0, 0), u01 = u00, u10 = u00, u11 = u00;
+            if (ok00) u00 = ldg16(c00);
+            if (ok01) u01 = ldg16(c00 + rb);
+            if (ok10) u10 = ldg16(c00 + W * rb);
+            if (ok11) u11 = ldg16(c00 + (W + 1) * rb);
+            const float d00 = dot(u00, g), d01 = dot(u01, g), d10 = dot(u10, g),
+                        d11 = dot(u11, g);
+            const float wx0 = 1.f - fx, wy0 = 1.f - fy;
+            float gA = wy0 * (wx0 * d00 + fx * d01) + fy * (wx0 * d10 + fx * d11);
+            float gx = wy0 * (d01 - d00) + fy * (d11 - d10);
+            float gy = wx0 * (d10 - d00) + fx * (d11 - d01);
+            gA = group_sum<G>(gA);
+            gx = group_sum<G>(gx);
+            gy = group_sum<G>(gy);
+            if (active) {
+                if (sub == 0) {
+                    const bool any = ok00 || ok01 || ok10 || ok11;
+                    p.grad_attn[s] = gA;
+                    p.grad_loc[2 * s] = any ? a * gx * fW : 0.f;
+                    p.grad_loc[2 * s + 1] = any ? a * gy * fH : 0.f;
+                }
+                float *d = gl + r00 * rowf;
+                if (ok00) scatter<N>(d, a * (wy0 * wx0), g);
+                if (ok01) scatter<N>(d + rowf, a * (wy0 * fx), g);
+                if (ok10) scatter<N>(d + W * rowf, a * (fy * wx0), g);
+                if (ok11) scatter<N>(d + (W + 1) * rowf, a * (fy * fx), g);
+            }
+        }
+    }
+}
+
+template <int DT, int G, int LL, int PP>
+__global__ void __launch_bounds__(256)
+bwd3d_kernel(const __grid_constant__ Params p) {
+    constexpr int N = Vec<DT>::N;
+    const int L = LL > 0 ? LL : p.L;
+    const int P = PP > 0 ? PP : p.P;
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if ((t - (threadIdx.x & 31)) / G >= p.n_items) return;
+    long long item = t / G;
+    const bool active = item < p.n_items;
+    if (!active) item = p.n_items - 1;
+    const int sub = threadIdx.x & (G - 1);
+    const int m = static_cast<int>(item % p.M);
+    const long long b = item / p.M / p.Nq;
+    const long long rb = p.row_bytes;
+    const long long rowf = static_cast<long long>(p.M) * p.D;
+    const char *vb = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
+                     static_cast<long long>(m) * (rb / p.M) + sub * 16;
+    float *gvb = p.grad_value + (b * p.Nin) * rowf + static_cast<long long>(m) * p.D + sub * N;
+    float g[N];
+    unpack(ldg16(static_cast<const char *>(p.grad_out) + item * (rb / p.M) + sub * 16), g);
+    const long long s0 = item * L * P;
+
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+        const int W = p.W[l], H = p.H[l], Z = p.Z[l];
+        const float fW = p.fW[l], fH = p.fH[l], fZ = p.fZ[l];
+        const char *vl = vb + static_cast<long long>(p.start[l]) * rb;
+        float *gl = gvb + static_cast<long long>(p.start[l]) * rowf;
+        const long long HW = static_cast<long long>(H) * W;
+#pragma unroll 1
+        for (int k = 0; k < P; ++k) {
+            const long long s = s0 + l * P + k;
+            const float *xyz = p.loc + 3 * s;
+            const float a = __ldg(p.attn + s);
+            int x0, y0, z0;
+            float fx, fy, fz;
+            pixel_coord(__ldg(xyz), fW, x0, fx);
+            pixel_coord(__ldg(xyz + 1), fH, y0, fy);
+            pixel_coord(__ldg(xyz + 2), fZ, z0, fz);
+            const bool vx[2] = {x0 >= 0, x0 < W - 1};
+            const bool vy[2] = {y0 >= 0, y0 < H - 1};
+            const bool vz[2] = {z0 >= 0, z0 < Z - 1};
+            const float wx[2] = {1.f - fx, fx};
+            const float wy[2] = {1.f - fy, fy};
+            const float wz[2] = {1.f - fz, fz};
+            const long long r000 = static_cast<long long>((z0 * H + y0) * W + x0);
+            const char *c000 = vl + r000 * rb;
+            bool ok[8];
+            long long off[8];
+            float d[8];
+            bool any = false;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
+                ok[c] = vx[dx] && vy[dy] && vz[dz];
+                any = any || ok[c];
+                off[c] = dz * HW + dy * W + dx;
+                uint4 u = make_uint4(0, 0, 0, 0);
+                if (ok[c]) u = ldg16(c000 + off[c] * rb);
+                d[c] = dot(u, g);
+            }
+            float gA = 0.f, gx = 0.f, gy = 0.f, gz = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
+                const float sx = dx ? 1.f : -1.f, sy = dy ? 1.f : -1.f, sz = dz ? 1.f : -1.f;
+                gA = fmaf(wz[dz] * wy[dy] * wx[dx], d[c], gA);
+                gx = fmaf(sx * wz[dz] * wy[dy], d[c], gx);
+                gy = fmaf(sy * wz[dz] * wx[dx], d[c], gy);
+                gz = fmaf(sz * wy[dy] * wx[dx], d[c], gz);
+            }
+            gA = group_sum<G>(gA);
+            gx = group_sum<G>(gx);
+            gy = group_sum<G>(gy);
+            gz = group_sum<G>(gz);
+            if (active) {
+                if (sub == 0) {
+                    p.grad_attn[s] = gA;
+                    p.grad_loc[3 * s] = any ? a * gx * fW : 0.f;
+                    p.grad_loc[3 * s + 1] = any ? a * gy * fH : 0.f;
+                    p.grad_loc[3 * s + 2] = any ? a * gz * fZ : 0.f;
+                }
+                float *dst = gl + r000 * rowf;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
+                    if (ok[c]) scatter<N>(dst + off[c] * rowf, a * (wz[dz] * wy[dy] * wx[dx]), g);
+                }
+            }
+        }
+    }
+}
+
+template <int DT, int G>
+cudaError_t backward_lp(int ndim, const Params &p, cudaStream_t s) {
+    const long long threads = p.n_items * G;
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(blocks)), block(256);
+    if (ndim == 2) {
+        if (p.L == 4 && p.P == 4) bwd2d_kernel<DT, G, 4, 4><<<grid, block, 0, s>>>(p);
+        else if (p.L == 1 && p.P == 4) bwd2d_kernel<DT, G, 1, 4><<<grid, block, 0, s>>>(p);
+        else bwd2d_kernel<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
+    } else {
+        if (p.L == 4 && p.P == 4) bwd3d_kernel<DT, G, 4, 4><<<grid, block, 0, s>>>(p);
+        else bwd3d_kernel<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_zero_fill(float *ptr, long long n_floats, cudaStream_t s) {
+    if (n_floats <= 0) return cudaSuccess;
+    const long long n4 = n_floats / 4;  // rows are whole multiples of 16 bytes
+    long long blocks = (n4 + 255) / 256;
+    if (blocks > 148LL * 16) blocks = 148LL * 16;
+    zero_fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        reinterpret_cast<float4 *>(ptr), n4);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_backward(int ndim, int dtype, int G, const Params &p, cudaStream_t s) {
+    if (p.n_items == 0) return cudaSuccess;
+#define MSDA_BWD_CASE(DT, GG) \
+    if (dtype == DT && G == GG) return backward_lp<DT, GG>(ndim, p, s);
+    MSDA_BWD_CASE(kF32, 1) MSDA_BWD_CASE(kF32, 2) MSDA_BWD_CASE(kF32, 4)
+    MSDA_BWD_CASE(kF32, 8) MSDA_BWD_CASE(kF32, 16) MSDA_BWD_CASE(kF32, 32)
+    MSDA_BWD_CASE(kBF16, 1) MSDA_BWD_CASE(kBF16, 2) MSDA_BWD_CASE(kBF16, 4)
+    MSDA_BWD_CASE(kBF16, 8) MSDA_BWD_CASE(kBF16, 16) MSDA_BWD_CASE(kBF16, 32)
+#undef MSDA_BWD_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace msda

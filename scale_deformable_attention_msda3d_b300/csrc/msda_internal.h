@@ -1,0 +1,42 @@
+// Internal interface between the C-ABI layer (msda_abi.cpp) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace msda {
+
+constexpr int kF32 = 0;
+constexpr int kBF16 = 1;
+constexpr int kMaxLevels = 16;
+constexpr int kMaxPoints = 32;
+
+// Everything a kernel needs, passed by value as a __grid_constant__ parameter.
+// All level geometry is validated on the host before it gets here.
+struct Params {
+    // tensors
+    const void *value;          // [B, Nin, M, D]
+    const float *loc;           // [B, Nq, M, L, P, NDIM]
+    const float *attn;          // [B, Nq, M, L, P]
+    void *out;                  // [B, Nq, M*D]           (forward)
+    const void *grad_out;       // [B, Nq, M*D]           (backward)
+    float *grad_value;          // [B, Nin, M, D]         (backward)
+    float *grad_loc;            // like loc               (backward)
+    float *grad_attn;           // like attn              (backward)
+    // sizes
+    long long B, Nin, Nq;
+    long long n_items;          // B * Nq * M work items (b, q, m)
+    int M, D, L, P;
+    long long row_bytes;        // M * D * sizeof(value dtype): stride between value rows
+    // level geometry (entries >= L unused)
+    int W[kMaxLevels], H[kMaxLevels], Z[kMaxLevels], start[kMaxLevels];
+    float fW[kMaxLevels], fH[kMaxLevels], fZ[kMaxLevels];
+};
+
+// Launchers: enqueue on `stream`, return the launch status.  dtype is kF32 / kBF16,
+// G = D * sizeof(dtype) / 16 lanes per work item.
+cudaError_t launch_forward(int ndim, int dtype, int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_backward(int ndim, int dtype, int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_zero_fill(float *ptr, long long n_floats, cudaStream_t stream);
+
+}  // namespace msda

@@ -1,0 +1,175 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the device.
+
+Every call here either fails validation or is an empty no-op, so no CUDA API call is
+made; pointer arguments are plain integers that are never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import scale_deformable_attention_msda3d_b300 as msda
+from scale_deformable_attention_msda3d_b300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msda.h")
+
+FAKE = 0x10000          # 16-byte aligned, never dereferenced
+FAKE_MIS = 0x10004      # misaligned
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(msda\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return msda.load()
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(_binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # and through a fresh handle with plain dlopen semantics
+    raw = ctypes.CDLL(msda.library_path())
+    for name in declared_functions():
+        getattr(raw, name)
+
+
+def test_abi_version(lib):
+    assert msda.msda_abi_version() == 10000
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        _binding.load(str(tmp_path / "no_such_libmsda.so"))
+
+
+SH2 = np.array([[4, 6], [2, 3]], dtype=np.int64)
+LS2 = np.array([0, 24], dtype=np.int64)
+SH3 = np.array([[2, 4, 6], [1, 2, 3]], dtype=np.int64)
+LS3 = np.array([0, 48], dtype=np.int64)
+
+
+def dims(**kw):
+    d = dict(B=2, Nin=30, Nq=5, M=2, D=8, L=2, P=4, value_dtype=msda.MSDA_F32)
+    d.update(kw)
+    return msda.make_dims(**d)
+
+
+def fwd(nd=2, d=None, sh=None, ls=None, ptrs=None):
+    d = d or (dims() if nd == 2 else dims(Nin=54))
+    sh = SH2 if (sh is None and nd == 2) else (SH3 if sh is None else sh)
+    ls = LS2 if (ls is None and nd == 2) else (LS3 if ls is None else ls)
+    p = dict(value=FAKE, loc=FAKE, attn=FAKE, out=FAKE)
+    p.update(ptrs or {})
+    return msda.forward_raw(nd, d, p["value"], sh, ls, p["loc"], p["attn"], p["out"], 0)
+
+
+def bwd(nd=2, d=None, ptrs=None):
+    d = d or dims()
+    p = dict(value=FAKE, loc=FAKE, attn=FAKE, go=FAKE, gv=FAKE, gl=FAKE, ga=FAKE)
+    p.update(ptrs or {})
+    return msda.backward_raw(nd, d, p["value"], SH2, LS2, p["loc"], p["attn"], p["go"],
+                             p["gv"], p["gl"], p["ga"], 0)
+
+
+@pytest.mark.parametrize("case,status,msg", [
+    (dict(d=dims(value_dtype=7)), msda.MSDA_ERR_INVALID_ARG, "value_dtype"),
+    (dict(d=dims(Nq=-1)), msda.MSDA_ERR_INVALID_ARG, ">= 0"),
+    (dict(d=dims(M=0)), msda.MSDA_ERR_INVALID_ARG, ">= 1"),
+    (dict(d=dims(D=0)), msda.MSDA_ERR_INVALID_ARG, ">= 1"),
+    (dict(d=dims(L=17)), msda.MSDA_ERR_UNSUPPORTED, "MSDA_MAX_LEVELS"),
+    (dict(d=dims(P=33)), msda.MSDA_ERR_UNSUPPORTED, "MSDA_MAX_POINTS"),
+    (dict(d=dims(D=6)), msda.MSDA_ERR_UNSUPPORTED, "D * sizeof"),
+    (dict(d=dims(D=12)), msda.MSDA_ERR_UNSUPPORTED, "D * sizeof"),
+    (dict(d=dims(D=256)), msda.MSDA_ERR_UNSUPPORTED, "D * sizeof"),
+    (dict(d=dims(D=4, value_dtype=msda.MSDA_BF16)), msda.MSDA_ERR_UNSUPPORTED, "D * sizeof"),
+    (dict(d=dims(Nin=31)), msda.MSDA_ERR_INVALID_ARG, "add up to"),
+    (dict(ls=np.array([0, 23])), msda.MSDA_ERR_INVALID_ARG, "prefix sum"),
+    (dict(ls=np.array([1, 24])), msda.MSDA_ERR_INVALID_ARG, "prefix sum"),
+    (dict(sh=np.array([[4, 6], [0, 3]])), msda.MSDA_ERR_INVALID_ARG, "spatial_shapes"),
+    (dict(sh=np.array([[4, -6], [2, 3]])), msda.MSDA_ERR_INVALID_ARG, "spatial_shapes"),
+    (dict(d=dims(Nin=2 ** 31 + 5)), msda.MSDA_ERR_UNSUPPORTED, "2^31"),
+    (dict(ptrs=dict(value=0)), msda.MSDA_ERR_INVALID_ARG, "value is NULL"),
+    (dict(ptrs=dict(loc=0)), msda.MSDA_ERR_INVALID_ARG, "sampling_locations is NULL"),
+    (dict(ptrs=dict(attn=0)), msda.MSDA_ERR_INVALID_ARG, "attention_weights is NULL"),
+    (dict(ptrs=dict(out=0)), msda.MSDA_ERR_INVALID_ARG, "out is NULL"),
+    (dict(ptrs=dict(value=FAKE_MIS)), msda.MSDA_ERR_INVALID_ARG, "aligned"),
+    (dict(ptrs=dict(out=FAKE_MIS)), msda.MSDA_ERR_INVALID_ARG, "aligned"),
+])
+def test_forward_rejects_bad_arguments(lib, case, status, msg):
+    st = fwd(**case)
+    assert st == status, (st, msda.msda_last_error())
+    assert msg in msda.msda_last_error()
+
+
+def test_forward_3d_rejects_bad_arguments(lib):
+    assert fwd(nd=3, d=dims(Nin=54), sh=np.array([[2, 4, 6], [1, 2, 4]])) == \
+        msda.MSDA_ERR_INVALID_ARG
+    assert fwd(nd=3, d=dims(Nin=54), sh=np.array([[2, 4, 2 ** 24], [1, 2, 3]])) == \
+        msda.MSDA_ERR_INVALID_ARG
+
+
+def test_null_metadata_and_dims(lib):
+    d = dims()
+    fn = lib.msda2d_forward
+    st = fn(None, _binding._VP(FAKE), None, None, _binding._VP(FAKE), _binding._VP(FAKE),
+            _binding._VP(FAKE), _binding._VP(0))
+    assert st == msda.MSDA_ERR_INVALID_ARG and "dims" in msda.msda_last_error()
+    st = fn(ctypes.byref(d), _binding._VP(FAKE), None, None, _binding._VP(FAKE),
+            _binding._VP(FAKE), _binding._VP(FAKE), _binding._VP(0))
+    assert st == msda.MSDA_ERR_INVALID_ARG and "spatial_shapes" in msda.msda_last_error()
+
+
+@pytest.mark.parametrize("ptrs,msg", [
+    (dict(gv=0), "grad_value is NULL"), (dict(go=0), "grad_out is NULL"),
+    (dict(gl=FAKE_MIS), "grad_sampling_locations is not 16-byte aligned"),
+    (dict(ga=0), "grad_attention_weights is NULL"),
+])
+def test_backward_rejects_bad_arguments(lib, ptrs, msg):
+    st = bwd(ptrs=ptrs)
+    assert st == msda.MSDA_ERR_INVALID_ARG
+    assert msg in msda.msda_last_error()
+
+
+def test_empty_calls_are_ok_without_touching_the_device(lib):
+    # no queries: nothing to compute, null tensor pointers are fine
+    assert fwd(d=dims(Nq=0), ptrs=dict(value=0, loc=0, attn=0, out=0)) == msda.MSDA_OK
+    assert fwd(d=dims(B=0), ptrs=dict(value=0, loc=0, attn=0, out=0)) == msda.MSDA_OK
+    assert fwd(nd=3, d=dims(Nq=0, Nin=54)) == msda.MSDA_OK
+    # empty batch backward: no grad_value rows to zero
+    assert bwd(d=dims(B=0), ptrs=dict(gv=0, go=0)) == msda.MSDA_OK
+
+
+def test_error_message_is_per_thread(lib):
+    import threading
+    fwd(d=dims(M=0))
+    seen = {}
+
+    def other():
+        seen["msg"] = msda.msda_last_error()
+
+    t = threading.Thread(target=other)
+    t.start()
+    t.join()
+    assert seen["msg"] == ""
+    assert ">= 1" in msda.msda_last_error()
+
+
+def test_torch_layer_rejects_host_tensors():
+    torch = pytest.importorskip("torch")
+    v = torch.zeros(1, 24, 2, 8)
+    loc = torch.zeros(1, 3, 2, 1, 4, 2)
+    a = torch.zeros(1, 3, 2, 1, 4)
+    with pytest.raises(msda.MsdaError):
+        msda.msda2d_forward(v, np.array([[4, 6]]), np.array([0]), loc, a)

@@ -1,0 +1,224 @@
+"""CUDA path (libmsda through its C ABI) against the CPU oracle, element by element.
+
+Full-size runs of the five named workloads use the same binding call, kernels and launch
+configuration as bench.py.  Smaller cases cover every lane-group width (G = 1..32 lanes per
+row), the compiled (L, P) = (4, 4) / (1, 4) paths and the generic path, ragged tails
+(item counts that are not multiples of the warp / block tile), the largest L and P, and
+the edge cases: empty calls, a single query, exact gathers, non-finite and out-of-range
+locations, a non-default stream and the autograd wrapper.
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_parity import (check, check_backward, check_forward, device_inputs,
+                        grad_value_magnitude, host, run_backward, run_forward)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def msda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test ran without a CUDA device")
+    import scale_deformable_attention_msda3d_b300 as m
+    m.load()
+    return m
+
+
+def _named(name):
+    w = workloads.WORKLOADS[name]
+    return w, workloads.make_inputs(w)
+
+
+# ------------------------------------------------------------------ the named workloads
+
+
+def test_tiny2d_forward(msda):
+    w, inp = _named("tiny2d")
+    check_forward(msda, 2, inp, w.dtype, "tiny2d")
+
+
+def test_encoder2d_forward_full_size(msda):
+    w, inp = _named("encoder2d")
+    check_forward(msda, 2, inp, w.dtype, "encoder2d")
+
+
+def test_decoder2d_forward_bf16_full_size(msda):
+    w, inp = _named("decoder2d")
+    check_forward(msda, 2, inp, w.dtype, "decoder2d")
+
+
+def test_volume3d_forward_bf16_full_size(msda):
+    w, inp = _named("volume3d")
+    check_forward(msda, 3, inp, w.dtype, "volume3d")
+
+
+def test_encoder2d_backward_full_size(msda):
+    w, inp = _named("encoder2d_bwd")
+    check_backward(msda, 2, inp, w.dtype, "encoder2d_bwd")
+
+
+def test_encoder2d_backward_adjoint_identities(msda):
+    """sum(g * out) = sum(value * grad_value) = sum(A * grad_A), all from the GPU."""
+    w, inp = _named("encoder2d_bwd")
+    dev = device_inputs(inp, w.dtype)
+    out = host(run_forward(msda, 2, dev))
+    gv, gl, ga = (host(t) for t in run_backward(msda, 2, dev))
+    s_out = float((out * inp["grad_out"]).sum())
+    s_val = float((inp["value"].astype(np.float64) * gv).sum())
+    s_att = float((inp["attention_weights"].astype(np.float64) * ga).sum())
+    scale = float(np.abs(out * inp["grad_out"]).sum())
+    assert abs(s_out - s_val) <= 1e-5 * scale and abs(s_out - s_att) <= 1e-5 * scale
+
+
+def test_volume3d_backward_bf16_full_size(msda):
+    w, inp = _named("volume3d")
+    w = w.with_(backward=True)
+    inp = workloads.make_inputs(w)
+    check_backward(msda, 3, inp, w.dtype, "volume3d_bwd")
+
+
+# ------------------------------------------------------------------ coverage of shapes
+
+SHAPES2 = [(13, 17), (7, 5), (3, 4), (1, 2)]
+SHAPES3 = [(5, 6, 7), (3, 2, 4), (1, 3, 2)]
+
+CASES = [
+    # nd, dtype, D, L, P, B, Nq, M          (G = D * sizeof / 16)
+    (2, "f32", 4, 3, 5, 2, 1001, 3),        # G=1, generic (L, P)
+    (2, "f32", 8, 1, 4, 1, 257, 2),         # G=2, compiled (1, 4)
+    (2, "f32", 16, 4, 4, 2, 129, 5),        # G=4, compiled (4, 4)
+    (2, "f32", 32, 4, 4, 1, 77, 8),         # G=8, compiled (4, 4), ragged
+    (2, "f32", 64, 2, 3, 1, 45, 3),         # G=16
+    (2, "f32", 128, 1, 4, 2, 19, 2),        # G=32
+    (2, "bf16", 8, 4, 4, 2, 301, 3),        # G=1
+    (2, "bf16", 16, 2, 2, 1, 99, 4),        # G=2
+    (2, "bf16", 32, 4, 4, 3, 50, 8),        # G=4
+    (2, "bf16", 64, 1, 4, 1, 33, 2),        # G=8
+    (2, "bf16", 256, 2, 1, 1, 21, 1),       # G=32
+    (3, "f32", 16, 3, 3, 2, 201, 3),        # G=4, generic
+    (3, "f32", 32, 4, 4, 1, 65, 4),         # G=8, compiled (4, 4) -- 3D uses 4 levels
+    (3, "bf16", 32, 4, 4, 2, 130, 8),       # G=4
+    (3, "bf16", 8, 1, 4, 1, 97, 2),         # G=1, compiled (1, 4)
+    (3, "f32", 128, 2, 2, 1, 9, 1),         # G=32
+]
+
+
+def _shapes_for(nd, L):
+    base = SHAPES2 if nd == 2 else SHAPES3
+    return [base[i % len(base)] for i in range(L)]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[
+    f"{c[0]}d-{c[1]}-D{c[2]}-L{c[3]}-P{c[4]}-B{c[5]}-Nq{c[6]}-M{c[7]}" for c in CASES])
+def test_forward_and_backward_shapes(msda, case):
+    nd, dtype, D, L, P, B, Nq, M = case
+    inp = workloads.random_problem(nd, _shapes_for(nd, L), B=B, Nq=Nq, M=M, D=D, P=P,
+                                   dtype=dtype, seed=zlib.crc32(repr(case).encode()))
+    check_forward(msda, nd, inp, dtype, f"fwd {case}")
+    check_backward(msda, nd, inp, dtype, f"bwd {case}")
+
+
+def test_maximum_levels_and_points(msda):
+    shapes = [(3 + (l % 4), 2 + (l % 3)) for l in range(16)]
+    inp = workloads.random_problem(2, shapes, B=1, Nq=33, M=2, D=8, P=32, seed=5)
+    check_forward(msda, 2, inp, "f32", "L16 P32 fwd")
+    check_backward(msda, 2, inp, "f32", "L16 P32 bwd")
+
+
+def test_maximum_channels(msda):
+    inp = workloads.random_problem(2, [(9, 11)], B=1, Nq=40, M=1, D=256, P=4, dtype="bf16",
+                                   seed=6)
+    check_forward(msda, 2, inp, "bf16", "bf16 D=256")
+    inp = workloads.random_problem(3, [(3, 4, 5)], B=1, Nq=40, M=2, D=128, P=4, seed=7)
+    check_forward(msda, 3, inp, "f32", "3d f32 D=128")
+
+
+# ------------------------------------------------------------------ edge cases
+
+
+def test_exact_gather_is_bit_exact(msda):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    H = W = 16
+    B, Nq, M, D, P = 1, 300, 4, 32, 4
+    value = rng.standard_normal((B, H * W, M, D), dtype=np.float32)
+    ix = rng.integers(0, W, size=(B, Nq, M, 1, P))
+    iy = rng.integers(0, H, size=(B, Nq, M, 1, P))
+    loc = np.stack([(ix + 0.5) / W, (iy + 0.5) / H], -1).astype(np.float32)
+    attn = np.zeros((B, Nq, M, 1, P), dtype=np.float32)
+    attn[..., 1] = 1.0
+    inp = dict(value=value, spatial_shapes=np.array([[H, W]]), level_start_index=np.array([0]),
+               sampling_locations=loc, attention_weights=attn)
+    out = host(run_forward(msda, 2, device_inputs(inp, "f32"))).reshape(Nq, M, D)
+    rows = (iy[0, :, :, 0, 1] * W + ix[0, :, :, 0, 1])
+    want = np.stack([value[0, rows[:, m], m] for m in range(M)], 1)
+    assert np.array_equal(out, want.astype(np.float64))
+
+
+@pytest.mark.parametrize("nd", [2, 3])
+def test_non_finite_and_out_of_range_locations(msda, nd):
+    shapes = _shapes_for(nd, 2)
+    inp = workloads.random_problem(nd, shapes, B=1, Nq=64, M=2, D=8, P=4, seed=12)
+    loc = inp["sampling_locations"]
+    specials = [np.nan, np.inf, -np.inf, 3.0e38, -3.0e38, -0.75, 1.75, 0.0, 1.0]
+    for i, v in enumerate(specials):
+        loc[0, i, :, :, :, i % nd] = v
+    check_forward(msda, nd, inp, "f32", f"{nd}d specials fwd")
+    check_backward(msda, nd, inp, "f32", f"{nd}d specials bwd")
+    ref = oracle.run_inputs(nd, inp)
+    assert np.all(ref[0, 0:3] == 0.0)
+
+
+def test_empty_calls(msda):
+    torch = pytest.importorskip("torch")
+    inp = workloads.random_problem(2, SHAPES2[:2], B=2, Nq=0, M=2, D=8, P=4, seed=13)
+    dev = device_inputs(inp, "f32")
+    out = run_forward(msda, 2, dev)
+    assert tuple(out.shape) == (2, 0, 16)
+    gv = torch.full(tuple(dev["value"].shape), 7.0, device="cuda")
+    gv, gl, ga = msda.msda2d_backward(dev["value"], inp["spatial_shapes"],
+                                      inp["level_start_index"], dev["sampling_locations"],
+                                      dev["attention_weights"], dev["grad_out"], grad_value=gv)
+    torch.cuda.synchronize()
+    assert float(gv.abs().max()) == 0.0          # no queries: the value gradient is zero
+
+
+def test_single_query_single_head(msda):
+    inp = workloads.random_problem(2, SHAPES2, B=1, Nq=1, M=1, D=32, P=4, seed=14)
+    check_forward(msda, 2, inp, "f32", "1 query")
+    check_backward(msda, 2, inp, "f32", "1 query")
+
+
+def test_non_default_stream(msda):
+    torch = pytest.importorskip("torch")
+    inp = workloads.random_problem(2, SHAPES2, B=2, Nq=500, M=4, D=32, P=4, seed=15)
+    dev = device_inputs(inp, "f32")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        out = msda.msda2d_forward(dev["value"], inp["spatial_shapes"],
+                                  inp["level_start_index"], dev["sampling_locations"],
+                                  dev["attention_weights"])
+    s.synchronize()
+    check(host(out), oracle.run_inputs(2, inp), "f32", "side stream")
+
+
+def test_autograd_wrapper_matches_backward_call(msda):
+    torch = pytest.importorskip("torch")
+    inp = workloads.random_problem(2, SHAPES2, B=1, Nq=40, M=2, D=16, P=4, seed=16)
+    dev = device_inputs(inp, "f32")
+    v = dev["value"].clone().requires_grad_(True)
+    loc = dev["sampling_locations"].clone().requires_grad_(True)
+    a = dev["attention_weights"].clone().requires_grad_(True)
+    out = msda.ms_deform_attn(v, inp["spatial_shapes"], inp["level_start_index"], loc, a)
+    (out * dev["grad_out"]).sum().backward()
+    rgv, rgl, rga = oracle.run_inputs(2, inp, backward_pass=True)
+    check(host(v.grad), rgv, "f32", "autograd grad_value", mag=grad_value_magnitude(2, inp))
+    check(host(loc.grad), rgl, "f32", "autograd grad_loc")
+    check(host(a.grad), rga, "f32", "autograd grad_attn")

@@ -234,3 +234,40 @@ def shard_range(total: int, rank: int, world: int) -> Tuple[int, int]:
 
 def names() -> List[str]:
     return list(WORKLOADS)
+
+
+def random_problem(ndim: int, shapes: Sequence[Sequence[int]], B: int = 2, Nq: int = 37,
+                   M: int = 3, D: int = 8, P: int = 4, dtype: str = "f32", seed: int = 0,
+                   margin: float = 1.5, backward: bool = True) -> Dict[str, np.ndarray]:
+    """A small random problem in the ``make_inputs`` layout, for parity and edge tests.
+
+    Pixel coordinates are uniform over [-margin, extent - 1 + margin] on every axis, so a
+    share of the samples straddles or leaves the level (zero padding is exercised).
+    """
+    rng = np.random.default_rng(seed)
+    shapes = [tuple(int(e) for e in s) for s in shapes]
+    L = len(shapes)
+    Nin = int(sum(int(np.prod(s)) for s in shapes))
+    v32 = rng.standard_normal((B, Nin, M, D), dtype=np.float32)
+    out: Dict[str, np.ndarray] = {}
+    if dtype == "bf16":
+        out["value_bits"] = f32_to_bf16_bits(v32)
+        out["value"] = bf16_bits_to_f32(out["value_bits"])
+    else:
+        out["value"] = v32
+    out["spatial_shapes"] = np.array(shapes, dtype=np.int64).reshape(L, ndim)
+    out["level_start_index"] = level_start_index(shapes)
+    ext = np.stack([_extent_xyz(s) for s in shapes], 0)               # [L, ndim]
+    u = rng.random((B, Nq, M, L, P, ndim))
+    pix = u * (ext[None, None, None, :, None, :] - 1.0 + 2 * margin) - margin
+    out["sampling_locations"] = ((pix + 0.5) / ext[None, None, None, :, None, :]).astype(
+        np.float32)
+    out["attention_weights"] = _softmax_last(
+        rng.standard_normal((B, Nq, M, L * P))).reshape(B, Nq, M, L, P)
+    if backward:
+        g = rng.standard_normal((B, Nq, M * D), dtype=np.float32)
+        if dtype == "bf16":
+            out["grad_out_bits"] = f32_to_bf16_bits(g)
+            g = bf16_bits_to_f32(out["grad_out_bits"])
+        out["grad_out"] = g
+    return out
