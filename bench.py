@@ -226,24 +226,30 @@ def barrier(world):
         dist.barrier()
 
 
-def all_max(x: float, world: int) -> float:
+def _reduce(x: float, world: int, op: str) -> float:
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def all_max(x: float, world: int) -> float:
+    return _reduce(x, world, "max")
 
 
 def all_sum(x: float, world: int) -> float:
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(x, world, "sum")
+
+
+def aggregate(t_rank_s: float, samples_rank: int, steps: int, world: int):
+    """Whole-job throughput: samples of all ranks over the slowest rank's time."""
+    t_max = all_max(t_rank_s, world)
+    samples_all = all_sum(float(samples_rank), world) * steps
+    return samples_all / t_max, t_max
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -360,9 +366,7 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
     barrier(world)
     t_rank = ev0.elapsed_time(ev1) / 1e3                      # seconds, this rank
-    t_max = all_max(t_rank, world)
-    samples_all = all_sum(float(w.samples), world) * args.steps
-    value = samples_all / t_max
+    value, t_max = aggregate(t_rank, w.samples, args.steps, world)
     ms_per_step = t_max * 1e3 / args.steps
 
     # end to end through the public binding, host buffers, copies inside the timed region
@@ -468,9 +472,8 @@ def run_e2e(msda, w, inp, dev, args, world):
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t0
     t = max(ev0.elapsed_time(ev1) / 1e3, 0.0)
-    t_max = all_max(max(t, wall), world)
-    samples_all = all_sum(float(w.samples), world) * steps
-    return {"value": samples_all / t_max, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+    value, t_max = aggregate(max(t, wall), w.samples, steps, world)
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": t_max * 1e3 / steps,
             "path": "pinned host -> device copies, libmsda call, device -> pinned host copy, "

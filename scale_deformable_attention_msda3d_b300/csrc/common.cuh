@@ -64,8 +64,10 @@ __device__ __forceinline__ uint4 pack(const float (&v)[8]) {
 // the subtraction into one FMA, which would lose the error term.
 //
 // A coordinate that is not finite or lies at or beyond -1 / the extent is reported as
-// invalid (every corner outside); the outputs are then i0 = -2, frac = 0, so all corner
-// tests fail and no weight is NaN.
+// invalid (the function returns false; i0 = -2 and frac = 0 so no weight is NaN).  The
+// caller ANDs the flags of all axes into every corner test: i0 = -2 alone does not fail
+// the upper-bound test of the far corner.  When the flag is true, i0 is in [-1, extent-1],
+// so a corner that passes its bound tests addresses a pixel inside the level.
 __device__ __forceinline__ bool pixel_coord(float loc, float extent, int &i0, float &frac) {
     const float prod = __fmul_rn(loc, extent);
     const float err = __fmaf_rn(loc, extent, -prod);

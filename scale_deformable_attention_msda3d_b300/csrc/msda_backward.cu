@@ -78,9 +78,10 @@ bwd2d_kernel(const __grid_constant__ Params p) {
             const float a = __ldg(p.attn + s);
             int x0, y0;
             float fx, fy;
-            pixel_coord(xy.x, fW, x0, fx);
-            pixel_coord(xy.y, fH, y0, fy);
-            const bool vx0 = x0 >= 0, vx1 = x0 < W - 1;
+            const bool okx = pixel_coord(xy.x, fW, x0, fx);
+            const bool oky = pixel_coord(xy.y, fH, y0, fy);
+            const bool ok = okx && oky;
+            const bool vx0 = ok && x0 >= 0, vx1 = ok && x0 < W - 1;
             const bool vy0 = y0 >= 0, vy1 = y0 < H - 1;
             const bool ok00 = vy0 && vx0, ok01 = vy0 && vx1, ok10 = vy1 && vx0, ok11 = vy1 && vx1;
             const long long r00 = static_cast<long long>(y0 * W + x0);
@@ -153,10 +154,10 @@ bwd3d_kernel(const __grid_constant__ Params p) {
             const float a = __ldg(p.attn + s);
             int x0, y0, z0;
             float fx, fy, fz;
-            pixel_coord(__ldg(xyz), fW, x0, fx);
-            pixel_coord(__ldg(xyz + 1), fH, y0, fy);
-            pixel_coord(__ldg(xyz + 2), fZ, z0, fz);
-            const bool vx[2] = {x0 >= 0, x0 < W - 1};
+            const bool ok = pixel_coord(__ldg(xyz), fW, x0, fx) &
+                            pixel_coord(__ldg(xyz + 1), fH, y0, fy) &
+                            pixel_coord(__ldg(xyz + 2), fZ, z0, fz);
+            const bool vx[2] = {ok && x0 >= 0, ok && x0 < W - 1};
             const bool vy[2] = {y0 >= 0, y0 < H - 1};
             const bool vz[2] = {z0 >= 0, z0 < Z - 1};
             const float wx[2] = {1.f - fx, fx};

@@ -48,9 +48,10 @@ fwd2d_kernel(const __grid_constant__ Params p) {
             const float a = __ldg(ap + l * P + k);
             int x0, y0;
             float fx, fy;
-            pixel_coord(xy.x, fW, x0, fx);
-            pixel_coord(xy.y, fH, y0, fy);
-            const bool vx0 = x0 >= 0, vx1 = x0 < W - 1;
+            const bool okx = pixel_coord(xy.x, fW, x0, fx);
+            const bool oky = pixel_coord(xy.y, fH, y0, fy);
+            const bool ok = okx && oky;
+            const bool vx0 = ok && x0 >= 0, vx1 = ok && x0 < W - 1;
             const bool vy0 = y0 >= 0, vy1 = y0 < H - 1;
             const float ay0 = a * (1.f - fy), ay1 = a * fy;
             const float w00 = (vy0 && vx0) ? ay0 * (1.f - fx) : 0.f;
@@ -117,10 +118,9 @@ fwd3d_kernel(const __grid_constant__ Params p) {
             const float a = __ldg(ap + l * P + k);
             int x0, y0, z0;
             float fx, fy, fz;
-            pixel_coord(lx, fW, x0, fx);
-            pixel_coord(ly, fH, y0, fy);
-            pixel_coord(lz, fZ, z0, fz);
-            const bool vx[2] = {x0 >= 0, x0 < W - 1};
+            const bool ok = pixel_coord(lx, fW, x0, fx) & pixel_coord(ly, fH, y0, fy) &
+                            pixel_coord(lz, fZ, z0, fz);
+            const bool vx[2] = {ok && x0 >= 0, ok && x0 < W - 1};
             const bool vy[2] = {y0 >= 0, y0 < H - 1};
             const bool vz[2] = {z0 >= 0, z0 < Z - 1};
             const float wx[2] = {1.f - fx, fx};
@@ -132,10 +132,10 @@ fwd3d_kernel(const __grid_constant__ Params p) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
-                const bool ok = vx[dx] && vy[dy] && vz[dz];
-                w[c] = ok ? wz[dz] * wy[dy] * wx[dx] : 0.f;
+                const bool inside = vx[dx] && vy[dy] && vz[dz];
+                w[c] = inside ? wz[dz] * wy[dy] * wx[dx] : 0.f;
                 u[c] = make_uint4(0, 0, 0, 0);
-                if (ok) u[c] = ldg16(c000 + dz * sz + dy * sy + dx * rb);
+                if (inside) u[c] = ldg16(c000 + dz * sz + dy * sy + dx * rb);
             }
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
