@@ -14,8 +14,6 @@ from typing import Optional, Sequence, Tuple, Union
 
 import numpy as np
 
-from . import build as _build
-
 MSDA_OK, MSDA_ERR_INVALID_ARG, MSDA_ERR_UNSUPPORTED, MSDA_ERR_CUDA, MSDA_ERR_INTERNAL = range(5)
 MSDA_F32, MSDA_BF16 = 0, 1
 MSDA_MAX_LEVELS = 16
@@ -48,8 +46,13 @@ _I64P = ctypes.POINTER(ctypes.c_int64)
 _DIMS_P = ctypes.POINTER(msda_dims)
 
 
+def _builder():
+    from . import build
+    return build
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _builder().LIB
 
 
 def load(path: Optional[str] = None):
@@ -59,7 +62,7 @@ def load(path: Optional[str] = None):
         if _lib is not None and path is None:
             return _lib
         if path is None:
-            path = _build.build()
+            path = _builder().build()
         if not os.path.exists(path):
             raise RuntimeError(f"libmsda not found at {path}")
         lib = ctypes.CDLL(path)
@@ -75,7 +78,7 @@ def load(path: Optional[str] = None):
         lib.msda_last_error.restype = ctypes.c_char_p
         lib.msda_abi_version.argtypes = []
         lib.msda_abi_version.restype = ctypes.c_int32
-        if path == _build.LIB:
+        if path == _builder().LIB:
             _lib = lib
         return lib
 

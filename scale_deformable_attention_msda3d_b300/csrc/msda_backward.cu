@@ -154,10 +154,10 @@ bwd3d_kernel(const __grid_constant__ Params p) {
             const float a = __ldg(p.attn + s);
             int x0, y0, z0;
             float fx, fy, fz;
-            const bool ok = pixel_coord(__ldg(xyz), fW, x0, fx) &
-                            pixel_coord(__ldg(xyz + 1), fH, y0, fy) &
-                            pixel_coord(__ldg(xyz + 2), fZ, z0, fz);
-            const bool vx[2] = {ok && x0 >= 0, ok && x0 < W - 1};
+            const bool valid = pixel_coord(__ldg(xyz), fW, x0, fx) &
+                               pixel_coord(__ldg(xyz + 1), fH, y0, fy) &
+                               pixel_coord(__ldg(xyz + 2), fZ, z0, fz);
+            const bool vx[2] = {valid && x0 >= 0, valid && x0 < W - 1};
             const bool vy[2] = {y0 >= 0, y0 < H - 1};
             const bool vz[2] = {z0 >= 0, z0 < Z - 1};
             const float wx[2] = {1.f - fx, fx};
