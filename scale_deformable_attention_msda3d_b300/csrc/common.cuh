@@ -54,12 +54,17 @@ __device__ __forceinline__ uint4 pack(const float (&v)[8]) {
 }
 
 // Normalised location -> pixel coordinate on one axis: x = loc * extent - 0.5
-// (align_corners = false).  Returns the cell index floor(x) and the fraction x - floor(x).
+// (align_corners = false).  Returns the cell index floor(x) and the fraction x - floor(x)
+// of the EXACT coordinate, not of its fp32 rounding:
 //
-// The product loc * extent is rounded once to fp32 and its exact rounding error is
-// recovered with an FMA and folded into the fraction, so the fraction is accurate to about
-// 1e-7 of a pixel relative to the exact double-precision coordinate, independent of the
-// extent.  (Rounding x itself to fp32 would cost up to ~8e-6 px at extent 150.)
+// * the product loc * extent is rounded once and its exact rounding error `err` is
+//   recovered with an FMA; prod - 0.5 is exact for prod in [0.25, 2^23);
+// * the fraction (x - floor(x)) + err is moved into [0, 1] by shifting the cell by one
+//   when the error carries the coordinate across an integer.  The cell then agrees with
+//   floor() of the exact coordinate, which matters for the location gradient: it jumps at
+//   integer coordinates (the right-hand derivative of the cell chosen by floor() is used).
+//   Rounding x itself to fp32 would also cost up to ~8e-6 px of accuracy at extent 150.
+//
 // Intrinsics with explicit rounding keep the compiler from contracting the product and
 // the subtraction into one FMA, which would lose the error term.
 //
@@ -72,9 +77,18 @@ __device__ __forceinline__ bool pixel_coord(float loc, float extent, int &i0, fl
     const float prod = __fmul_rn(loc, extent);
     const float err = __fmaf_rn(loc, extent, -prod);
     const float x = __fsub_rn(prod, 0.5f);
-    const bool ok = (x > -1.0f) && (x < extent);
-    const float xf = floorf(x);
-    frac = ok ? __fadd_rn(__fsub_rn(x, xf), err) : 0.0f;
+    float xf = floorf(x);
+    float f = __fadd_rn(__fsub_rn(x, xf), err);
+    if (f < 0.0f) {
+        xf = __fsub_rn(xf, 1.0f);
+        f = __fadd_rn(f, 1.0f);
+    } else if (f >= 1.0f) {
+        xf = __fadd_rn(xf, 1.0f);
+        f = __fsub_rn(f, 1.0f);
+    }
+    // exact coordinate = xf + f with f in [0, 1]; it lies in (-1, extent) iff:
+    const bool ok = (xf >= -1.0f) && (xf < extent) && (xf > -1.0f || f > 0.0f);
+    frac = ok ? f : 0.0f;
     i0 = ok ? static_cast<int>(xf) : -2;
     return ok;
 }
