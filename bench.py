@@ -139,7 +139,8 @@ def algorithmic_bytes(w: workloads.Workload, inp) -> dict:
 
 
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while the GPU works."""
+    """Samples SM clock and clock-event (throttle) reasons while the GPU works: through
+    NVML when pynvml imports, else by running nvidia-smi in loop mode."""
 
     REASONS = {
         "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
@@ -148,58 +149,109 @@ class ClockSampler:
         "display_clock_setting": 0x100,
     }
 
-    def __init__(self, device_index: int, period_s: float = 0.005):
+    def __init__(self, device_index: int, pci_bus_id: str = None, period_s: float = 0.005):
         self.samples = []
         self.reasons = set()
         self.max_mhz = None
         self.period = period_s
+        self.source = None
+        self.error = None
         self._stop = threading.Event()
         self._t = None
+        self._proc = None
+        self._smi_id = pci_bus_id or str(device_index)
         try:
             import pynvml
             pynvml.nvmlInit()
             self._nvml = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self._h = (pynvml.nvmlDeviceGetHandleByPciBusId(pci_bus_id) if pci_bus_id
+                       else pynvml.nvmlDeviceGetHandleByIndex(device_index))
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # NVML missing: report no clocks rather than guess
+            self.source = "nvml"
+        except Exception as e:
             self._nvml = None
-            self.error = str(e)
+            self.error = f"pynvml: {e}"
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.source = "nvidia-smi"
+
+    def _add(self, mhz, max_mhz, mask):
+        self.samples.append(float(mhz))
+        if max_mhz:
+            self.max_mhz = float(max_mhz)
+        for name, bit in self.REASONS.items():
+            if mask & bit:
+                self.reasons.add(name)
 
     def sample_once(self):
         if self._nvml is None:
             return
         n = self._nvml
         try:
-            self.samples.append(n.nvmlDeviceGetClockInfo(self._h, n.NVML_CLOCK_SM))
-            r = n.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-            for name, bit in self.REASONS.items():
-                if r & bit:
-                    self.reasons.add(name)
+            self._add(n.nvmlDeviceGetClockInfo(self._h, n.NVML_CLOCK_SM), None,
+                      n.nvmlDeviceGetCurrentClocksEventReasons(self._h))
         except Exception:
             pass
 
-    def _run(self):
+    def _run_nvml(self):
         while not self._stop.is_set():
             self.sample_once()
             time.sleep(self.period)
 
+    def _run_smi(self):
+        for line in self._proc.stdout:
+            parts = [t.strip() for t in line.split(",")]
+            if len(parts) != 3:
+                continue
+            try:
+                self._add(float(parts[0]), float(parts[1]), int(parts[2], 16))
+            except ValueError:
+                continue
+
     def __enter__(self):
-        if self._nvml is not None:
-            self._t = threading.Thread(target=self._run, daemon=True)
+        if self.source == "nvml":
+            self._t = threading.Thread(target=self._run_nvml, daemon=True)
             self._t.start()
+        elif self.source == "nvidia-smi":
+            import subprocess
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self._smi_id,
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._run_smi, daemon=True)
+            self._t.start()
+            time.sleep(0.3)          # let the first samples arrive before the timed work
         return self
 
     def __exit__(self, *a):
         self._stop.set()
+        if self._proc is not None:
+            time.sleep(0.05)
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
         if self._t is not None:
-            self._t.join()
+            self._t.join(timeout=5)
 
     def summary(self):
-        if self._nvml is None:
+        if self.source is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.error}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
-                "reasons": sorted(self.reasons - {"gpu_idle"})}
+                "reasons": sorted(self.reasons - {"gpu_idle"}), "source": self.source}
+
+
+def pci_bus_id(dev) -> str:
+    """nvidia-smi / NVML style bus id of a torch CUDA device (None if unknown)."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -351,7 +403,7 @@ def run_ours(args):
             step(i)
     torch.cuda.synchronize(dev)
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, pci_bus_id(dev))
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
