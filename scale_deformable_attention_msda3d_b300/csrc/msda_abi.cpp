@@ -46,8 +46,8 @@ msda_status build_params(const msda_dims *d, int ndim, const int64_t *shapes,
     if (d->P > MSDA_MAX_POINTS)
         return fail(MSDA_ERR_UNSUPPORTED, "P = %d exceeds MSDA_MAX_POINTS = %d", d->P,
                     MSDA_MAX_POINTS);
-    if (d->Nin > INT32_MAX)
-        return fail(MSDA_ERR_UNSUPPORTED, "Nin = %lld must be below 2^31", (long long)d->Nin);
+    if (d->Nin > (int64_t(1) << 30))
+        return fail(MSDA_ERR_UNSUPPORTED, "Nin = %lld must be at most 2^30", (long long)d->Nin);
     if (!shapes || !level_start)
         return fail(MSDA_ERR_INVALID_ARG, "spatial_shapes / level_start_index is NULL");
 
@@ -58,6 +58,9 @@ msda_status build_params(const msda_dims *d, int ndim, const int64_t *shapes,
                     "D * sizeof(dtype) = %lld bytes; supported: 16, 32, 64, 128, 256, 512",
                     (long long)dbytes);
     *G = int(dbytes / 16);
+    if (int64_t(d->M) * dbytes > INT32_MAX)
+        return fail(MSDA_ERR_UNSUPPORTED, "M * D * sizeof(dtype) = %lld bytes must be below 2^31",
+                    (long long)(int64_t(d->M) * dbytes));
 
     int64_t total = 0;
     for (int l = 0; l < d->L; ++l) {
@@ -68,7 +71,7 @@ msda_status build_params(const msda_dims *d, int ndim, const int64_t *shapes,
                 return fail(MSDA_ERR_INVALID_ARG,
                             "spatial_shapes[%d][%d] = %lld must be in [1, 2^24)", l, k,
                             (long long)e);
-            if (!mul_ok(size, e, &size) || size > INT32_MAX)
+            if (!mul_ok(size, e, &size) || size > (int64_t(1) << 30))
                 return fail(MSDA_ERR_INVALID_ARG, "level %d has too many pixels", l);
         }
         if (level_start[l] != total)
@@ -101,6 +104,7 @@ msda_status build_params(const msda_dims *d, int ndim, const int64_t *shapes,
     p->P = d->P;
     p->n_items = items;
     p->row_bytes = int64_t(d->M) * dbytes;
+    p->rb32 = int(p->row_bytes);
     for (int l = 0; l < d->L; ++l) {
         const int64_t *s = shapes + l * ndim;
         p->W[l] = int(s[ndim - 1]);
@@ -110,6 +114,8 @@ msda_status build_params(const msda_dims *d, int ndim, const int64_t *shapes,
         p->fH[l] = float(p->H[l]);
         p->fZ[l] = float(p->Z[l]);
         p->start[l] = int(level_start[l]);
+        p->sy[l] = int64_t(p->W[l]) * p->row_bytes;
+        p->sz[l] = int64_t(p->H[l]) * p->W[l] * p->row_bytes;
     }
     return MSDA_OK;
 }

@@ -5,10 +5,18 @@
 // changes from "3D Attention That Knows Where to Look").
 //
 // Mapping: a lane group of G lanes per (b, q, m) work item; lane k owns 16 bytes of
-// channels.  Per sample the group computes the cell and corner weights redundantly
-// (cheap ALU), then issues one predicated 16-byte load per existing corner: a warp-wide
-// load brings 32/G whole value rows.  Corners outside the level are neither loaded nor
-// weighted.  fp32 accumulation; one store of the item's D channels at the end.
+// channels, so a warp-wide 16-byte load brings 32/G whole value rows.  Corners outside
+// the level are neither loaded nor weighted.  fp32 accumulation; one store of the item's
+// D channels at the end.
+//
+// Two kernels:
+// * fwd_tiled (the compiled (L, P) pairs): the locations and weights of an item are read
+//   once with vector loads, spread over the lanes of its group; each lane works out the
+//   cell, corner validity and weights of its own samples, and the group then walks the
+//   samples in order, taking each sample's corner data from its owner by warp shuffle.
+//   Optionally the item's samples are split over SPLIT lane groups whose partial sums are
+//   added by shuffles at the end (more loads in flight when there are few items).
+// * fwd{2,3}d_generic (any L, P): every lane of the group computes every sample itself.
 #include "common.cuh"
 
 namespace msda {
@@ -17,7 +25,7 @@ namespace {
 
 template <int DT, int G, int LL, int PP>
 __global__ void __launch_bounds__(256)
-fwd2d_kernel(const __grid_constant__ Params p) {
+fwd2d_generic(const __grid_constant__ Params p) {
     constexpr int N = Vec<DT>::N;
     const int L = LL > 0 ? LL : p.L;
     const int P = PP > 0 ? PP : p.P;
@@ -85,7 +93,7 @@ fwd2d_kernel(const __grid_constant__ Params p) {
 
 template <int DT, int G, int LL, int PP>
 __global__ void __launch_bounds__(256)
-fwd3d_kernel(const __grid_constant__ Params p) {
+fwd3d_generic(const __grid_constant__ Params p) {
     constexpr int N = Vec<DT>::N;
     const int L = LL > 0 ? LL : p.L;
     const int P = PP > 0 ? PP : p.P;
@@ -150,21 +158,259 @@ fwd3d_kernel(const __grid_constant__ Params p) {
     *reinterpret_cast<uint4 *>(o) = pack(acc);
 }
 
+
+// ------------------------------------------------------------------ compiled (L, P)
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Corner data of one sample: value row of corner 0 (relative to the item's batch), one
+// validity bit per corner (bit c: corner c lies inside the level) and the corner weights
+// with the attention weight folded in (0 for corners outside).  Corner c has offsets
+// dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2.
+template <int NC> struct Taps {
+    int row;
+    unsigned ok;
+    float w[NC];
+};
+
+__device__ __forceinline__ void make_taps(const Params &p, int l, const float *xy, float a,
+                                          Taps<4> &t) {
+    int x0, y0;
+    float fx, fy;
+    const bool ok = pixel_coord(xy[0], p.fW[l], x0, fx) & pixel_coord(xy[1], p.fH[l], y0, fy);
+    const int W = p.W[l], H = p.H[l];
+    const bool vx0 = ok && x0 >= 0, vx1 = ok && x0 < W - 1;
+    const bool vy0 = y0 >= 0, vy1 = y0 < H - 1;
+    t.ok = unsigned(vy0 && vx0) | unsigned(vy0 && vx1) << 1 | unsigned(vy1 && vx0) << 2 |
+           unsigned(vy1 && vx1) << 3;
+    const float ay0 = a * (1.f - fy), ay1 = a * fy;
+    t.w[0] = (t.ok & 1u) ? ay0 * (1.f - fx) : 0.f;
+    t.w[1] = (t.ok & 2u) ? ay0 * fx : 0.f;
+    t.w[2] = (t.ok & 4u) ? ay1 * (1.f - fx) : 0.f;
+    t.w[3] = (t.ok & 8u) ? ay1 * fx : 0.f;
+    t.row = ok ? p.start[l] + y0 * W + x0 : 0;
+}
+
+__device__ __forceinline__ void make_taps(const Params &p, int l, const float *xyz, float a,
+                                          Taps<8> &t) {
+    int x0, y0, z0;
+    float fx, fy, fz;
+    const bool ok = pixel_coord(xyz[0], p.fW[l], x0, fx) & pixel_coord(xyz[1], p.fH[l], y0, fy) &
+                    pixel_coord(xyz[2], p.fZ[l], z0, fz);
+    const int W = p.W[l], H = p.H[l], Z = p.Z[l];
+    const bool vx[2] = {ok && x0 >= 0, ok && x0 < W - 1};
+    const bool vy[2] = {y0 >= 0, y0 < H - 1};
+    const bool vz[2] = {z0 >= 0, z0 < Z - 1};
+    const float wx[2] = {1.f - fx, fx};
+    const float wy[2] = {1.f - fy, fy};
+    const float wz[2] = {a * (1.f - fz), a * fz};
+    t.ok = 0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
+        const bool in = vx[dx] && vy[dy] && vz[dz];
+        t.ok |= unsigned(in) << c;
+        t.w[c] = in ? (wz[dz] * wy[dy]) * wx[dx] : 0.f;
+    }
+    t.row = ok ? p.start[l] + (z0 * H + y0) * W + x0 : 0;
+}
+
+// Largest of 4, 2, 1 floats dividing x (alignment of a float offset, in floats).
+__host__ __device__ constexpr int falign(int x) { return x % 4 == 0 ? 4 : (x % 2 == 0 ? 2 : 1); }
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+// K consecutive floats starting at a pointer aligned to A floats, read once (streaming).
+template <int K, int A>
+__device__ __forceinline__ void load_stream(const float *src, float (&r)[K]) {
+    if constexpr (A == 4 && K % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < K / 4; ++i) {
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(src) + i);
+            r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+        }
+    } else if constexpr (A >= 2 && K % 2 == 0) {
+#pragma unroll
+        for (int i = 0; i < K / 2; ++i) {
+            const float2 v = __ldcs(reinterpret_cast<const float2 *>(src) + i);
+            r[2 * i] = v.x; r[2 * i + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < K; ++i) r[i] = __ldcs(src + i);
+    }
+}
+
+// acc += w * (the N channels in u), with packed fp32x2 FMAs (same rounding as fmaf).
+template <int N>
+__device__ __forceinline__ void fma_row(float2 (&acc)[N / 2], float w, const uint4 &u) {
+    float v[N];
+    unpack(u, v);
+    const float2 w2 = make_float2(w, w);
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) acc[i] = __ffma2_rn(w2, make_float2(v[2 * i], v[2 * i + 1]), acc[i]);
+}
+
+template <int NC>
+__device__ __forceinline__ Taps<NC> shfl_taps(const Taps<NC> &t, int src, int width) {
+    Taps<NC> r;
+    r.row = __shfl_sync(kFull, t.row, src, width);
+    r.ok = __shfl_sync(kFull, t.ok, src, width);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) r.w[c] = __shfl_sync(kFull, t.w[c], src, width);
+    return r;
+}
+
+// One item = (b, q, m); LANES = G * SPLIT lanes per item; lane = (item, sp, sub).
+// Subgroup sp handles samples [sp * SS, (sp + 1) * SS) of the item (sample index
+// l * P + p); its lane `sub` computes the taps of SPL of them.
+template <int DT, int G, int NDIM, int LL, int PP, int SPLIT>
+__global__ void __launch_bounds__(256)
+fwd_tiled(const __grid_constant__ Params p) {
+    constexpr int N = Vec<DT>::N;
+    constexpr int NC = 1 << NDIM;
+    constexpr int S = LL * PP;
+    static_assert(S % SPLIT == 0, "SPLIT must divide L * P");
+    constexpr int SS = S / SPLIT;
+    constexpr int SPL = (SS + G - 1) / G;
+    constexpr int LANES = G * SPLIT;
+    static_assert(LANES <= 32 && (32 % LANES) == 0, "lanes per item must divide the warp");
+    // when every lane owns exactly SPL samples, read them with vector loads
+    constexpr bool EVEN = (SS % G) == 0;
+    constexpr int ALOC = cmin(cmin(falign(S * NDIM), falign(SS * NDIM)), falign(SPL * NDIM));
+    constexpr int AATT = cmin(cmin(falign(S), falign(SS)), falign(SPL));
+
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    // whole warps leave together: the shuffles below need every lane of the warp
+    if ((t & ~31LL) / LANES >= p.n_items) return;
+    long long item = t / LANES;
+    const bool active = item < p.n_items;
+    if (!active) item = p.n_items - 1;  // tail lanes redo a real item and store nothing
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & (G - 1);
+    const int sp = SPLIT > 1 ? (lane / G) & (SPLIT - 1) : 0;
+    const int m = static_cast<int>(item % p.M);
+    const long long b = item / p.M / p.Nq;
+    const int s0 = sp * SS;                  // first sample of this subgroup
+    const int my0 = s0 + sub * SPL;          // first sample whose taps this lane computes
+
+    // 1. locations and weights of this lane's samples, then their taps
+    float lv[SPL * NDIM], av[SPL];
+    const float *lsrc = p.loc + (item * S + my0) * NDIM;
+    const float *asrc = p.attn + item * S + my0;
+    if constexpr (EVEN) {
+        load_stream<SPL * NDIM, ALOC>(lsrc, lv);
+        load_stream<SPL, AATT>(asrc, av);
+    } else {
+#pragma unroll
+        for (int i = 0; i < SPL; ++i) {
+            const bool have = sub * SPL + i < SS;
+#pragma unroll
+            for (int k = 0; k < NDIM; ++k) lv[i * NDIM + k] = have ? __ldcs(lsrc + i * NDIM + k) : 0.f;
+            av[i] = have ? __ldcs(asrc + i) : 0.f;
+        }
+    }
+    Taps<NC> tp[SPL];
+#pragma unroll
+    for (int i = 0; i < SPL; ++i) {
+        // a lane past the end of the subgroup's samples computes a harmless copy of
+        // sample my0 clamped into range (never shuffled out)
+        const int j = cmin(my0 + i, s0 + SS - 1);
+        make_taps(p, j / PP, lv + i * NDIM, av[i], tp[i]);
+    }
+
+    // 2. walk the subgroup's samples; corner rows are 16-byte slices per lane
+    const long long rb = p.row_bytes;
+    const char *vb = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
+                     static_cast<long long>(m) * (rb / p.M) + sub * 16;
+    float2 acc[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < SS; ++s) {
+        const Taps<NC> tt = shfl_taps(tp[s % SPL], s / SPL, G);
+        const int l = (s0 + s) / PP;  // a constant when SPLIT == 1
+        const char *c0 = vb + static_cast<long long>(tt.row) * p.rb32;
+        uint4 u[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
+            long long off = dx ? rb : 0;
+            if (dy) off += p.sy[l];
+            if (dz) off += p.sz[l];
+            u[c] = make_uint4(0, 0, 0, 0);
+            if (tt.ok & (1u << c)) u[c] = ldg16(c0 + off);
+        }
+#pragma unroll
+        for (int c = 0; c < NC; ++c) fma_row<N>(acc, tt.w[c], u[c]);
+    }
+
+    // 3. add the subgroups' partial sums, store the item's channels
+    if constexpr (SPLIT > 1) {
+#pragma unroll
+        for (int o = G; o < LANES; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                acc[i].x += __shfl_xor_sync(kFull, acc[i].x, o);
+                acc[i].y += __shfl_xor_sync(kFull, acc[i].y, o);
+            }
+    }
+    if (active && sp == 0) {
+        float r[N];
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) { r[2 * i] = acc[i].x; r[2 * i + 1] = acc[i].y; }
+        char *o = static_cast<char *>(p.out) + item * (rb / p.M) + sub * 16;
+        __stcs(reinterpret_cast<uint4 *>(o), pack(r));
+    }
+}
+
+// Lane groups per item for the compiled path: split an item's samples over more lanes
+// while the launch would otherwise leave the GPU short of resident warps.
+template <int G, int S>
+int pick_split(long long n_items) {
+    constexpr long long kWantThreads = 148LL * 2048 * 2;  // two full waves of the B300's SMs
+    int split = 1;
+    while (split < 4 && G * split * 2 <= 32 && S % (split * 2) == 0 &&
+           n_items * G * split < kWantThreads)
+        split *= 2;
+    return split;
+}
+
+template <int DT, int G, int NDIM, int LL, int PP, int SPLIT>
+cudaError_t launch_tiled(const Params &p, cudaStream_t s) {
+    const long long threads = p.n_items * G * SPLIT;
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    fwd_tiled<DT, G, NDIM, LL, PP, SPLIT><<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int DT, int G, int NDIM, int LL, int PP>
+cudaError_t launch_tiled_split(const Params &p, cudaStream_t s) {
+    const int split = pick_split<G, LL * PP>(p.n_items);
+    if constexpr (G <= 16) {
+        if (split == 2) return launch_tiled<DT, G, NDIM, LL, PP, 2>(p, s);
+    }
+    if constexpr (G <= 8) {
+        if (split == 4) return launch_tiled<DT, G, NDIM, LL, PP, 4>(p, s);
+    }
+    return launch_tiled<DT, G, NDIM, LL, PP, 1>(p, s);
+}
+
 template <int DT, int G>
 cudaError_t forward_lp(int ndim, const Params &p, cudaStream_t s) {
+    if (ndim == 2) {
+        if (p.L == 4 && p.P == 4) return launch_tiled_split<DT, G, 2, 4, 4>(p, s);
+        if (p.L == 1 && p.P == 4) return launch_tiled_split<DT, G, 2, 1, 4>(p, s);
+    } else {
+        if (p.L == 4 && p.P == 4) return launch_tiled_split<DT, G, 3, 4, 4>(p, s);
+        if (p.L == 1 && p.P == 4) return launch_tiled_split<DT, G, 3, 1, 4>(p, s);
+    }
     const long long threads = p.n_items * G;
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>(blocks)), block(256);
-    if (ndim == 2) {
-        if (p.L == 4 && p.P == 4) fwd2d_kernel<DT, G, 4, 4><<<grid, block, 0, s>>>(p);
-        else if (p.L == 1 && p.P == 4) fwd2d_kernel<DT, G, 1, 4><<<grid, block, 0, s>>>(p);
-        else fwd2d_kernel<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
-    } else {
-        if (p.L == 4 && p.P == 4) fwd3d_kernel<DT, G, 4, 4><<<grid, block, 0, s>>>(p);
-        else if (p.L == 1 && p.P == 4) fwd3d_kernel<DT, G, 1, 4><<<grid, block, 0, s>>>(p);
-        else fwd3d_kernel<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
-    }
+    if (ndim == 2) fwd2d_generic<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
+    else fwd3d_generic<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
     return cudaGetLastError();
 }
 

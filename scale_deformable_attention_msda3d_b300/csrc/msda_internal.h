@@ -28,9 +28,12 @@ struct Params {
     long long n_items;          // B * Nq * M work items (b, q, m)
     int M, D, L, P;
     long long row_bytes;        // M * D * sizeof(value dtype): stride between value rows
+    int rb32;                   // row_bytes as a 32-bit int (validated to fit)
     // level geometry (entries >= L unused)
     int W[kMaxLevels], H[kMaxLevels], Z[kMaxLevels], start[kMaxLevels];
     float fW[kMaxLevels], fH[kMaxLevels], fZ[kMaxLevels];
+    long long sy[kMaxLevels];   // bytes between value rows one image row apart (W * row_bytes)
+    long long sz[kMaxLevels];   // bytes between value rows one slice apart (H * W * row_bytes)
 };
 
 // Launchers: enqueue on `stream`, return the launch status.  dtype is kF32 / kBF16,

@@ -99,7 +99,7 @@ def bwd(nd=2, d=None, ptrs=None):
     (dict(ls=np.array([1, 24])), msda.MSDA_ERR_INVALID_ARG, "prefix sum"),
     (dict(sh=np.array([[4, 6], [0, 3]])), msda.MSDA_ERR_INVALID_ARG, "spatial_shapes"),
     (dict(sh=np.array([[4, -6], [2, 3]])), msda.MSDA_ERR_INVALID_ARG, "spatial_shapes"),
-    (dict(d=dims(Nin=2 ** 31 + 5)), msda.MSDA_ERR_UNSUPPORTED, "2^31"),
+    (dict(d=dims(Nin=2 ** 30 + 5)), msda.MSDA_ERR_UNSUPPORTED, "2^30"),
     (dict(ptrs=dict(value=0)), msda.MSDA_ERR_INVALID_ARG, "value is NULL"),
     (dict(ptrs=dict(loc=0)), msda.MSDA_ERR_INVALID_ARG, "sampling_locations is NULL"),
     (dict(ptrs=dict(attn=0)), msda.MSDA_ERR_INVALID_ARG, "attention_weights is NULL"),
