@@ -93,6 +93,15 @@ __device__ __forceinline__ bool pixel_coord(float loc, float extent, int &i0, fl
     return ok;
 }
 
+// Read-only 32-byte load (one 256-bit access; sm_100 and later).  `volatile` keeps the
+// compiler from hoisting it above the caller's bounds test.
+__device__ __forceinline__ void ldg32(const void *p, uint4 &a, uint4 &b) {
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
+                   "=r"(b.w)
+                 : "l"(p));
+}
+
 // Vector reduction of 4 fp32 values into global memory (no return value).
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
     atomicAdd(reinterpret_cast<float4 *>(addr), make_float4(a, b, c, d));

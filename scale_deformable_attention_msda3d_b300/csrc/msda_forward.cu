@@ -13,9 +13,11 @@
 // * fwd_tiled (the compiled (L, P) pairs): the locations and weights of an item are read
 //   once with vector loads, spread over the lanes of its group; each lane works out the
 //   cell, corner validity and weights of its own samples, and the group then walks the
-//   samples in order, taking each sample's corner data from its owner by warp shuffle.
+//   samples in order, taking each sample's corner data from its owner by warp shuffle and
+//   loading the corner rows of the next AHEAD samples before summing the current one.
 //   Optionally the item's samples are split over SPLIT lane groups whose partial sums are
-//   added by shuffles at the end (more loads in flight when there are few items).
+//   added by shuffles at the end (fewer taps per lane for narrow rows, more loads in flight
+//   when there are few items).  3D uses 32-byte (256-bit) loads per lane.
 // * fwd{2,3}d_generic (any L, P): every lane of the group computes every sample itself.
 #include "common.cuh"
 
@@ -240,14 +242,47 @@ __device__ __forceinline__ void load_stream(const float *src, float (&r)[K]) {
     }
 }
 
-// acc += w * (the N channels in u), with packed fp32x2 FMAs (same rounding as fmaf).
-template <int N>
-__device__ __forceinline__ void fma_row(float2 (&acc)[N / 2], float w, const uint4 &u) {
-    float v[N];
+// VB bytes of one value row held by one lane (16: one 128-bit load; 32: one 256-bit load).
+template <int VB> struct Slice;
+template <> struct Slice<16> { uint4 a; };
+template <> struct Slice<32> { uint4 a, b; };
+
+__device__ __forceinline__ void load_slice(const char *p, Slice<16> &r) { r.a = ldg16(p); }
+__device__ __forceinline__ void load_slice(const char *p, Slice<32> &r) { ldg32(p, r.a, r.b); }
+__device__ __forceinline__ void zero_slice(Slice<16> &r) { r.a = make_uint4(0, 0, 0, 0); }
+__device__ __forceinline__ void zero_slice(Slice<32> &r) {
+    r.a = make_uint4(0, 0, 0, 0);
+    r.b = r.a;
+}
+
+// acc += w * (the channels of one 16-byte piece), packed fp32x2 FMAs (same rounding as fmaf).
+template <int DT>
+__device__ __forceinline__ void fma16(float2 *acc, float w, const uint4 &u) {
+    constexpr int NV = Vec<DT>::N;
+    float v[NV];
     unpack(u, v);
     const float2 w2 = make_float2(w, w);
 #pragma unroll
-    for (int i = 0; i < N / 2; ++i) acc[i] = __ffma2_rn(w2, make_float2(v[2 * i], v[2 * i + 1]), acc[i]);
+    for (int i = 0; i < NV / 2; ++i) acc[i] = __ffma2_rn(w2, make_float2(v[2 * i], v[2 * i + 1]), acc[i]);
+}
+
+template <int DT, int VB>
+__device__ __forceinline__ void fma_slice(float2 *acc, float w, const Slice<VB> &r) {
+    fma16<DT>(acc, w, r.a);
+    if constexpr (VB == 32) fma16<DT>(acc + Vec<DT>::N / 2, w, r.b);
+}
+
+// 16 bytes of output channels from acc[half * NV/2 ...] (bf16: one RNE rounding).
+template <int DT>
+__device__ __forceinline__ uint4 pack16(const float2 *acc) {
+    constexpr int NV = Vec<DT>::N;
+    float r[NV];
+#pragma unroll
+    for (int i = 0; i < NV / 2; ++i) {
+        r[2 * i] = acc[i].x;
+        r[2 * i + 1] = acc[i].y;
+    }
+    return pack(r);
 }
 
 template <int NC>
@@ -260,13 +295,26 @@ __device__ __forceinline__ Taps<NC> shfl_taps(const Taps<NC> &t, int src, int wi
     return r;
 }
 
+// Launch shape of the compiled path for one (ndim, dtype): bytes per lane and row (VB),
+// samples whose corner rows are in flight ahead of the one being summed (AHEAD), and the
+// minimum resident blocks per SM that caps registers (MINB).  Tuned on B300 with the
+// encoder (fp32 2D), decoder (bf16 2D) and volume (bf16 3D) workloads: the gather is bound
+// by how many corner rows are in flight per SM, so occupancy is worth more than depth in
+// 2D, while 3D's 8 corners per sample favour 256-bit loads and a deeper window.
+template <int NDIM, int DT> struct Shape;
+template <> struct Shape<2, kF32> { static constexpr int VB = 16, AHEAD = 1, MINB = 6; };
+template <> struct Shape<2, kBF16> { static constexpr int VB = 16, AHEAD = 1, MINB = 5; };
+template <> struct Shape<3, kF32> { static constexpr int VB = 32, AHEAD = 2, MINB = 2; };
+template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 2, MINB = 2; };
+
 // One item = (b, q, m); LANES = G * SPLIT lanes per item; lane = (item, sp, sub).
 // Subgroup sp handles samples [sp * SS, (sp + 1) * SS) of the item (sample index
-// l * P + p); its lane `sub` computes the taps of SPL of them.
-template <int DT, int G, int NDIM, int LL, int PP, int SPLIT>
-__global__ void __launch_bounds__(256)
+// l * P + p); its lane `sub` computes the taps of SPL of them.  The corner rows of the
+// next AHEAD samples are loaded before the current sample is summed.
+template <int DT, int G, int VB, int NDIM, int LL, int PP, int SPLIT, int AHEAD, int MINB>
+__global__ void __launch_bounds__(256, MINB)
 fwd_tiled(const __grid_constant__ Params p) {
-    constexpr int N = Vec<DT>::N;
+    constexpr int N = VB / Vec<DT>::ESIZE;  // channels per lane
     constexpr int NC = 1 << NDIM;
     constexpr int S = LL * PP;
     static_assert(S % SPLIT == 0, "SPLIT must divide L * P");
@@ -278,6 +326,7 @@ fwd_tiled(const __grid_constant__ Params p) {
     constexpr bool EVEN = (SS % G) == 0;
     constexpr int ALOC = cmin(cmin(falign(S * NDIM), falign(SS * NDIM)), falign(SPL * NDIM));
     constexpr int AATT = cmin(cmin(falign(S), falign(SS)), falign(SPL));
+    constexpr int DEPTH = AHEAD + 1;
 
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     // whole warps leave together: the shuffles below need every lane of the warp
@@ -318,30 +367,40 @@ fwd_tiled(const __grid_constant__ Params p) {
         make_taps(p, j / PP, lv + i * NDIM, av[i], tp[i]);
     }
 
-    // 2. walk the subgroup's samples; corner rows are 16-byte slices per lane
+    // 2. walk the subgroup's samples; corner rows are VB-byte slices per lane
     const long long rb = p.row_bytes;
     const char *vb = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
-                     static_cast<long long>(m) * (rb / p.M) + sub * 16;
+                     static_cast<long long>(m) * (rb / p.M) + sub * VB;
     float2 acc[N / 2];
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int s = 0; s < SS; ++s) {
-        const Taps<NC> tt = shfl_taps(tp[s % SPL], s / SPL, G);
+
+    Taps<NC> tq[DEPTH];
+    Slice<VB> u[DEPTH][NC];
+    // taps of sample s from its owner lane, and its in-level corner rows
+    auto fetch = [&](int s, int slot) {
+        tq[slot] = shfl_taps(tp[s % SPL], s / SPL, G);
         const int l = (s0 + s) / PP;  // a constant when SPLIT == 1
-        const char *c0 = vb + static_cast<long long>(tt.row) * p.rb32;
-        uint4 u[NC];
+        const char *c0 = vb + static_cast<long long>(tq[slot].row) * p.rb32;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
             long long off = dx ? rb : 0;
             if (dy) off += p.sy[l];
             if (dz) off += p.sz[l];
-            u[c] = make_uint4(0, 0, 0, 0);
-            if (tt.ok & (1u << c)) u[c] = ldg16(c0 + off);
+            zero_slice(u[slot][c]);
+            if (tq[slot].ok & (1u << c)) load_slice(c0 + off, u[slot][c]);
         }
+    };
 #pragma unroll
-        for (int c = 0; c < NC; ++c) fma_row<N>(acc, tt.w[c], u[c]);
+    for (int k = 0; k < AHEAD; ++k)
+        if (k < SS) fetch(k, k);
+#pragma unroll
+    for (int s = 0; s < SS; ++s) {
+        if (s + AHEAD < SS) fetch(s + AHEAD, (s + AHEAD) % DEPTH);
+        const int slot = s % DEPTH;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) fma_slice<DT, VB>(acc, tq[slot].w[c], u[slot][c]);
     }
 
     // 3. add the subgroups' partial sums, store the item's channels
@@ -355,38 +414,45 @@ fwd_tiled(const __grid_constant__ Params p) {
             }
     }
     if (active && sp == 0) {
-        float r[N];
-#pragma unroll
-        for (int i = 0; i < N / 2; ++i) { r[2 * i] = acc[i].x; r[2 * i + 1] = acc[i].y; }
-        char *o = static_cast<char *>(p.out) + item * (rb / p.M) + sub * 16;
-        __stcs(reinterpret_cast<uint4 *>(o), pack(r));
+        uint4 *o = reinterpret_cast<uint4 *>(static_cast<char *>(p.out) + item * (rb / p.M) + sub * VB);
+        __stcs(o, pack16<DT>(acc));
+        if constexpr (VB == 32) __stcs(o + 1, pack16<DT>(acc + Vec<DT>::N / 2));
     }
 }
 
-// Lane groups per item for the compiled path: split an item's samples over more lanes
-// while the launch would otherwise leave the GPU short of resident warps.
-template <int G, int S>
+// Lane groups per item for the compiled path.  Narrow rows (few lanes per row) split an
+// item's samples until one lane computes the taps of at most MAX_SPL samples (their
+// registers would spill otherwise); then the split grows while the launch would leave the
+// GPU short of resident warps.
+template <int G, int S, int NDIM>
 int pick_split(long long n_items) {
+    constexpr int MAX_SPL = NDIM == 2 ? 4 : 2;
     constexpr long long kWantThreads = 148LL * 2048 * 2;  // two full waves of the B300's SMs
+    auto can_double = [](int split) { return split < 4 && G * split * 2 <= 32 && S % (split * 2) == 0; };
     int split = 1;
-    while (split < 4 && G * split * 2 <= 32 && S % (split * 2) == 0 &&
-           n_items * G * split < kWantThreads)
-        split *= 2;
+    while (can_double(split) && S / split > MAX_SPL * G) split *= 2;
+    while (can_double(split) && n_items * G * split < kWantThreads) split *= 2;
     return split;
 }
 
 template <int DT, int G, int NDIM, int LL, int PP, int SPLIT>
 cudaError_t launch_tiled(const Params &p, cudaStream_t s) {
+    using SH = Shape<NDIM, DT>;
     const long long threads = p.n_items * G * SPLIT;
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    fwd_tiled<DT, G, NDIM, LL, PP, SPLIT><<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+    fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB>
+        <<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int DT, int G, int NDIM, int LL, int PP>
+// G16 = lanes per row at 16 bytes per lane; the kernel uses G = row bytes / VB lanes.
+template <int DT, int G16, int NDIM, int LL, int PP>
 cudaError_t launch_tiled_split(const Params &p, cudaStream_t s) {
-    const int split = pick_split<G, LL * PP>(p.n_items);
+    constexpr int VB = Shape<NDIM, DT>::VB;
+    constexpr int G = G16 * 16 / VB;
+    static_assert(G >= 1, "rows narrower than one lane's slice take the generic path");
+    const int split = pick_split<G, LL * PP, NDIM>(p.n_items);
     if constexpr (G <= 16) {
         if (split == 2) return launch_tiled<DT, G, NDIM, LL, PP, 2>(p, s);
     }
@@ -396,22 +462,24 @@ cudaError_t launch_tiled_split(const Params &p, cudaStream_t s) {
     return launch_tiled<DT, G, NDIM, LL, PP, 1>(p, s);
 }
 
-template <int DT, int G>
-cudaError_t forward_lp(int ndim, const Params &p, cudaStream_t s) {
-    if (ndim == 2) {
-        if (p.L == 4 && p.P == 4) return launch_tiled_split<DT, G, 2, 4, 4>(p, s);
-        if (p.L == 1 && p.P == 4) return launch_tiled_split<DT, G, 2, 1, 4>(p, s);
-    } else {
-        if (p.L == 4 && p.P == 4) return launch_tiled_split<DT, G, 3, 4, 4>(p, s);
-        if (p.L == 1 && p.P == 4) return launch_tiled_split<DT, G, 3, 1, 4>(p, s);
+template <int DT, int G, int NDIM>
+cudaError_t forward_nd(const Params &p, cudaStream_t s) {
+    if constexpr (G * 16 >= Shape<NDIM, DT>::VB) {
+        if (p.L == 4 && p.P == 4) return launch_tiled_split<DT, G, NDIM, 4, 4>(p, s);
+        if (p.L == 1 && p.P == 4) return launch_tiled_split<DT, G, NDIM, 1, 4>(p, s);
     }
     const long long threads = p.n_items * G;
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>(blocks)), block(256);
-    if (ndim == 2) fwd2d_generic<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
+    if constexpr (NDIM == 2) fwd2d_generic<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
     else fwd3d_generic<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
     return cudaGetLastError();
+}
+
+template <int DT, int G>
+cudaError_t forward_lp(int ndim, const Params &p, cudaStream_t s) {
+    return ndim == 2 ? forward_nd<DT, G, 2>(p, s) : forward_nd<DT, G, 3>(p, s);
 }
 
 }  // namespace
