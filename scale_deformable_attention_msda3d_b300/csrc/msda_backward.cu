@@ -6,9 +6,19 @@
 //   grad_A        = sum_c w_c <g, v_c>
 //   grad_x (px)   = a * sum_c dw_c/dx <g, v_c>,   grad_loc_x = W_l * grad_x   (x = loc*W - 0.5)
 //   grad_value[c] += a * w_c * g                  (corners inside the level only)
-// The lane group recomputes the sample, forms per-lane partial dot products over its 16
-// bytes of channels, reduces grad_A / grad_loc with xor shuffles inside the group, and
-// scatters grad_value with 16-byte vector reductions (red.global.add.v4.f32).
+//
+// Two kernels:
+// * bwd_tiled (the compiled (L, P) pairs).  A CTA handles one (batch, head) and a run of
+//   queries; a lane group of G lanes (16 bytes of channels each) handles one query.  Lane
+//   j of the group owns samples j, G + j, 2G + j, ...: it reads their locations and
+//   weights and computes their taps, which the group takes by shuffle.  Every lane forms
+//   its partial dot products <g, v_c> over its channels; after each batch of G samples a
+//   butterfly reduce-scatter leaves each sample's full dot products on its owner, which
+//   writes grad_A and grad_loc.  grad_value goes through 16-byte red.global.add.v4.f32.
+//   (Accumulating small levels in shared memory first was measured and dropped: on this
+//   part shared-memory fp32 atomics ran about ten times slower than the L2 reductions.)
+// * bwd{2,3}d_generic (any L, P): every lane of the group computes every sample, reduces
+//   grad_A / grad_loc with xor shuffles and scatters with red.global.add.v4.f32.
 #include "common.cuh"
 
 namespace msda {
@@ -42,7 +52,7 @@ __device__ __forceinline__ float dot(const uint4 &u, const float (&g)[N]) {
 
 template <int DT, int G, int LL, int PP>
 __global__ void __launch_bounds__(256)
-bwd2d_kernel(const __grid_constant__ Params p) {
+bwd2d_generic(const __grid_constant__ Params p) {
     constexpr int N = Vec<DT>::N;
     const int L = LL > 0 ? LL : p.L;
     const int P = PP > 0 ? PP : p.P;
@@ -119,7 +129,7 @@ bwd2d_kernel(const __grid_constant__ Params p) {
 
 template <int DT, int G, int LL, int PP>
 __global__ void __launch_bounds__(256)
-bwd3d_kernel(const __grid_constant__ Params p) {
+bwd3d_generic(const __grid_constant__ Params p) {
     constexpr int N = Vec<DT>::N;
     const int L = LL > 0 ? LL : p.L;
     const int P = PP > 0 ? PP : p.P;
@@ -211,21 +221,175 @@ bwd3d_kernel(const __grid_constant__ Params p) {
     }
 }
 
-template <int DT, int G>
-cudaError_t backward_lp(int ndim, const Params &p, cudaStream_t s) {
+// ------------------------------------------------------------------ compiled (L, P)
+
+// Sum over the G lanes of a group of v[j][k] (j = owner lane, k < K), scattered: lane
+// `sub` ends with the group's sums for owner sub in v[0][0..K-1].  (G - 1) * K shuffles.
+template <int G, int K>
+__device__ __forceinline__ void reduce_scatter(float (&v)[G][K], int sub) {
+#pragma unroll
+    for (int o = G / 2; o >= 1; o >>= 1) {
+        const bool hi = (sub & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i)
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const float send = hi ? v[i][k] : v[i + o][k];
+                const float keep = hi ? v[i + o][k] : v[i][k];
+                v[i][k] = keep + __shfl_xor_sync(kFull, send, o);
+            }
+    }
+}
+
+// grad_value += wgt * g over this lane's N channels of one corner row.
+template <int N>
+__device__ __forceinline__ void add_global(float *dst, float wgt, const float (&g)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4)
+        red_add_v4(dst + i, wgt * g[i], wgt * g[i + 1], wgt * g[i + 2], wgt * g[i + 3]);
+}
+template <int DT, int G, int NDIM, int LL, int PP, int BT>
+__global__ void __launch_bounds__(BT)
+bwd_tiled(const __grid_constant__ Params p) {
+    constexpr int N = Vec<DT>::N;  // channels per lane (16 bytes of value)
+    constexpr int NC = 1 << NDIM;
+    constexpr int S = LL * PP;
+    constexpr int NB = (S + G - 1) / G;  // batches of G samples per item
+    constexpr int GPB = BT / G;          // lane groups (queries in flight) per CTA
+
+    const int cta = blockIdx.x;
+    const int bm = cta / p.nchunk, chunk = cta - bm * p.nchunk;
+    const int m = bm % p.M;
+    const long long b = bm / p.M;
+    const long long q_lo = static_cast<long long>(chunk) * p.qchunk;
+    const long long q_hi = q_lo + p.qchunk < p.Nq ? q_lo + p.qchunk : p.Nq;
+    const int sub = threadIdx.x & (G - 1);
+    const int grp = threadIdx.x / G;
+    const int D = p.D;
+    const long long rb = p.row_bytes;
+    const long long rowf = static_cast<long long>(p.M) * D;  // grad_value row stride (floats)
+
+    const char *vbase = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
+                        static_cast<long long>(m) * (rb / p.M) + sub * 16;
+    float *gbase = p.grad_value + (b * p.Nin) * rowf + static_cast<long long>(m) * D + sub * N;
+    const int rounds = static_cast<int>((q_hi - q_lo + GPB - 1) / GPB);
+
+    for (int r = 0; r < rounds; ++r) {
+        long long q = q_lo + static_cast<long long>(r) * GPB + grp;
+        const bool active = q < q_hi;
+        if (!active) q = q_hi - 1;  // recompute a real query, write nothing
+        const long long item = (b * p.Nq + q) * p.M + m;
+        float g[N];
+        unpack(ldg16(static_cast<const char *>(p.grad_out) + item * (rb / p.M) + sub * 16), g);
+
+#pragma unroll
+        for (int bt = 0; bt < NB; ++bt) {
+            // taps of the sample this lane owns in this batch
+            const int own = bt * G + sub;
+            const bool owns = own < S;
+            const int so = owns ? own : S - 1;
+            float xyz[NDIM];
+#pragma unroll
+            for (int k = 0; k < NDIM; ++k) xyz[k] = __ldcs(p.loc + (item * S + so) * NDIM + k);
+            const float a = __ldcs(p.attn + item * S + so);
+            Taps<NC> mine;
+            float frac[NDIM];
+            make_taps(p, so / PP, xyz, a, mine, frac);
+
+            float dp[G][NC];  // partial <g, v_c> of every sample of the batch
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const int s = bt * G + j;
+                if (s >= S) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) dp[j][c] = 0.f;
+                    continue;
+                }
+                const Taps<NC> t = shfl_taps(mine, j, G);
+                const int l = s / PP;
+                const char *c0 = vbase + static_cast<long long>(t.row) * p.rb32;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
+                    long long off = dx ? rb : 0;
+                    if (dy) off += p.sy[l];
+                    if (dz) off += p.sz[l];
+                    uint4 u = make_uint4(0, 0, 0, 0);
+                    const bool in = (t.ok >> c) & 1u;
+                    if (in) u = ldg16(c0 + off);
+                    float v[N];
+                    unpack(u, v);
+                    float d = 0.f;
+#pragma unroll
+                    for (int i = 0; i < N; ++i) d = fmaf(g[i], v[i], d);
+                    dp[j][c] = d;
+                    if (active && in) {
+                        const int crow = t.row + dx + (dy ? p.W[l] : 0) + (dz ? p.W[l] * p.H[l] : 0);
+                        add_global<N>(gbase + static_cast<long long>(crow) * rowf, t.w[c], g);
+                    }
+                }
+            }
+            reduce_scatter<G, NC>(dp, sub);
+            if (active && owns) {
+                // dp[0][c] = <g, v_c> of sample `own`; corner weight derivatives from frac
+                const long long s = item * S + own;
+                float wx[2], wy[2], wz[2];
+                wx[0] = 1.f - frac[0]; wx[1] = frac[0];
+                wy[0] = 1.f - frac[1]; wy[1] = frac[1];
+                wz[0] = 1.f; wz[1] = 1.f;
+                if constexpr (NDIM == 3) { wz[0] = 1.f - frac[2]; wz[1] = frac[2]; }
+                float gA = 0.f, gx = 0.f, gy = 0.f, gz = 0.f;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
+                    const float d = dp[0][c];
+                    const float sx = dx ? 1.f : -1.f, sy = dy ? 1.f : -1.f, sz = dz ? 1.f : -1.f;
+                    gA = fmaf(wz[dz] * wy[dy] * wx[dx], d, gA);
+                    gx = fmaf(sx * wz[dz] * wy[dy], d, gx);
+                    gy = fmaf(sy * wz[dz] * wx[dx], d, gy);
+                    if constexpr (NDIM == 3) gz = fmaf(sz * wy[dy] * wx[dx], d, gz);
+                }
+                const bool any = mine.ok != 0u;
+                const int l = own / PP;
+                p.grad_attn[s] = gA;
+                p.grad_loc[NDIM * s] = any ? a * gx * p.fW[l] : 0.f;
+                p.grad_loc[NDIM * s + 1] = any ? a * gy * p.fH[l] : 0.f;
+                if constexpr (NDIM == 3) p.grad_loc[NDIM * s + 2] = any ? a * gz * p.fZ[l] : 0.f;
+            }
+        }
+    }
+
+}
+
+constexpr int kBwdBlock = 256;
+
+template <int DT, int G, int NDIM, int LL, int PP>
+cudaError_t launch_bwd_tiled(Params p, cudaStream_t s) {
+    // one round of lane groups per CTA: CTA = (b, m, run of kBwdBlock / G queries)
+    p.qchunk = kBwdBlock / G;
+    p.nchunk = static_cast<int>((p.Nq + p.qchunk - 1) / p.qchunk);
+    const long long ctas = p.B * p.M * p.nchunk;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    bwd_tiled<DT, G, NDIM, LL, PP, kBwdBlock><<<static_cast<unsigned>(ctas), kBwdBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int DT, int G, int NDIM>
+cudaError_t backward_nd(const Params &p, cudaStream_t s) {
+    if (p.L == 4 && p.P == 4) return launch_bwd_tiled<DT, G, NDIM, 4, 4>(p, s);
+    if (p.L == 1 && p.P == 4) return launch_bwd_tiled<DT, G, NDIM, 1, 4>(p, s);
     const long long threads = p.n_items * G;
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>(blocks)), block(256);
-    if (ndim == 2) {
-        if (p.L == 4 && p.P == 4) bwd2d_kernel<DT, G, 4, 4><<<grid, block, 0, s>>>(p);
-        else if (p.L == 1 && p.P == 4) bwd2d_kernel<DT, G, 1, 4><<<grid, block, 0, s>>>(p);
-        else bwd2d_kernel<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
-    } else {
-        if (p.L == 4 && p.P == 4) bwd3d_kernel<DT, G, 4, 4><<<grid, block, 0, s>>>(p);
-        else bwd3d_kernel<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
-    }
+    if constexpr (NDIM == 2) bwd2d_generic<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
+    else bwd3d_generic<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
     return cudaGetLastError();
+}
+
+template <int DT, int G>
+cudaError_t backward_lp(int ndim, const Params &p, cudaStream_t s) {
+    return ndim == 2 ? backward_nd<DT, G, 2>(p, s) : backward_nd<DT, G, 3>(p, s);
 }
 
 }  // namespace

@@ -163,85 +163,6 @@ fwd3d_generic(const __grid_constant__ Params p) {
 
 // ------------------------------------------------------------------ compiled (L, P)
 
-constexpr unsigned kFull = 0xffffffffu;
-
-// Corner data of one sample: value row of corner 0 (relative to the item's batch), one
-// validity bit per corner (bit c: corner c lies inside the level) and the corner weights
-// with the attention weight folded in (0 for corners outside).  Corner c has offsets
-// dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2.
-template <int NC> struct Taps {
-    int row;
-    unsigned ok;
-    float w[NC];
-};
-
-__device__ __forceinline__ void make_taps(const Params &p, int l, const float *xy, float a,
-                                          Taps<4> &t) {
-    int x0, y0;
-    float fx, fy;
-    const bool ok = pixel_coord(xy[0], p.fW[l], x0, fx) & pixel_coord(xy[1], p.fH[l], y0, fy);
-    const int W = p.W[l], H = p.H[l];
-    const bool vx0 = ok && x0 >= 0, vx1 = ok && x0 < W - 1;
-    const bool vy0 = y0 >= 0, vy1 = y0 < H - 1;
-    t.ok = unsigned(vy0 && vx0) | unsigned(vy0 && vx1) << 1 | unsigned(vy1 && vx0) << 2 |
-           unsigned(vy1 && vx1) << 3;
-    const float ay0 = a * (1.f - fy), ay1 = a * fy;
-    t.w[0] = (t.ok & 1u) ? ay0 * (1.f - fx) : 0.f;
-    t.w[1] = (t.ok & 2u) ? ay0 * fx : 0.f;
-    t.w[2] = (t.ok & 4u) ? ay1 * (1.f - fx) : 0.f;
-    t.w[3] = (t.ok & 8u) ? ay1 * fx : 0.f;
-    t.row = ok ? p.start[l] + y0 * W + x0 : 0;
-}
-
-__device__ __forceinline__ void make_taps(const Params &p, int l, const float *xyz, float a,
-                                          Taps<8> &t) {
-    int x0, y0, z0;
-    float fx, fy, fz;
-    const bool ok = pixel_coord(xyz[0], p.fW[l], x0, fx) & pixel_coord(xyz[1], p.fH[l], y0, fy) &
-                    pixel_coord(xyz[2], p.fZ[l], z0, fz);
-    const int W = p.W[l], H = p.H[l], Z = p.Z[l];
-    const bool vx[2] = {ok && x0 >= 0, ok && x0 < W - 1};
-    const bool vy[2] = {y0 >= 0, y0 < H - 1};
-    const bool vz[2] = {z0 >= 0, z0 < Z - 1};
-    const float wx[2] = {1.f - fx, fx};
-    const float wy[2] = {1.f - fy, fy};
-    const float wz[2] = {a * (1.f - fz), a * fz};
-    t.ok = 0;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
-        const bool in = vx[dx] && vy[dy] && vz[dz];
-        t.ok |= unsigned(in) << c;
-        t.w[c] = in ? (wz[dz] * wy[dy]) * wx[dx] : 0.f;
-    }
-    t.row = ok ? p.start[l] + (z0 * H + y0) * W + x0 : 0;
-}
-
-// Largest of 4, 2, 1 floats dividing x (alignment of a float offset, in floats).
-__host__ __device__ constexpr int falign(int x) { return x % 4 == 0 ? 4 : (x % 2 == 0 ? 2 : 1); }
-__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
-
-// K consecutive floats starting at a pointer aligned to A floats, read once (streaming).
-template <int K, int A>
-__device__ __forceinline__ void load_stream(const float *src, float (&r)[K]) {
-    if constexpr (A == 4 && K % 4 == 0) {
-#pragma unroll
-        for (int i = 0; i < K / 4; ++i) {
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(src) + i);
-            r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
-        }
-    } else if constexpr (A >= 2 && K % 2 == 0) {
-#pragma unroll
-        for (int i = 0; i < K / 2; ++i) {
-            const float2 v = __ldcs(reinterpret_cast<const float2 *>(src) + i);
-            r[2 * i] = v.x; r[2 * i + 1] = v.y;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < K; ++i) r[i] = __ldcs(src + i);
-    }
-}
-
 // VB bytes of one value row held by one lane (16: one 128-bit load; 32: one 256-bit load).
 template <int VB> struct Slice;
 template <> struct Slice<16> { uint4 a; };
@@ -283,16 +204,6 @@ __device__ __forceinline__ uint4 pack16(const float2 *acc) {
         r[2 * i + 1] = acc[i].y;
     }
     return pack(r);
-}
-
-template <int NC>
-__device__ __forceinline__ Taps<NC> shfl_taps(const Taps<NC> &t, int src, int width) {
-    Taps<NC> r;
-    r.row = __shfl_sync(kFull, t.row, src, width);
-    r.ok = __shfl_sync(kFull, t.ok, src, width);
-#pragma unroll
-    for (int c = 0; c < NC; ++c) r.w[c] = __shfl_sync(kFull, t.w[c], src, width);
-    return r;
 }
 
 // Launch shape of the compiled path for one (ndim, dtype): bytes per lane and row (VB),

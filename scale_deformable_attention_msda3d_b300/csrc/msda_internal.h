@@ -34,6 +34,9 @@ struct Params {
     float fW[kMaxLevels], fH[kMaxLevels], fZ[kMaxLevels];
     long long sy[kMaxLevels];   // bytes between value rows one image row apart (W * row_bytes)
     long long sz[kMaxLevels];   // bytes between value rows one slice apart (H * W * row_bytes)
+    // backward work split: CTA c handles batch b = c / (M * nchunk), head m = (c / nchunk) % M,
+    // and queries [chunk * qchunk, (chunk + 1) * qchunk) with chunk = c % nchunk
+    int nchunk, qchunk;
 };
 
 // Launchers: enqueue on `stream`, return the launch status.  dtype is kF32 / kBF16,
