@@ -326,9 +326,21 @@ def to_device(inp, w, dev):
     return d
 
 
-def make_step(msda, w, inp, bufs, stream):
-    """Returns step(i): one pass of the hot path on input set i % len(bufs)."""
+def make_step(msda, w, inp, bufs, stream, ordered=False):
+    """Returns step(i): one pass of the hot path on input set i % len(bufs).  With
+    `ordered`, each step first computes the locality-aware query order of its input set
+    (msda_query_order) and then runs the ordered forward, both inside the step."""
     shapes, starts = inp["spatial_shapes"], inp["level_start_index"]
+    if ordered:
+        fn = msda.msda2d_forward_ordered if w.ndim == 2 else msda.msda3d_forward_ordered
+
+        def step(i):
+            b = bufs[i % len(bufs)]
+            msda.msda_query_order(b["loc"], query_order=b["order"], workspace=b["ws"],
+                                  stream=stream)
+            fn(b["value"], shapes, starts, b["loc"], b["attn"], b["order"], out=b["out"],
+               stream=stream)
+        return step, 4          # keys, scan, scatter, forward (plus a histogram memset)
     if not w.backward:
         fn = msda.msda2d_forward if w.ndim == 2 else msda.msda3d_forward
 
@@ -395,9 +407,13 @@ def run_ours(args):
             b["gv"] = torch.empty(b["value"].shape, dtype=torch.float32, device=dev)
             b["gl"] = torch.empty_like(b["loc"])
             b["ga"] = torch.empty_like(b["attn"])
+        if args.order:
+            b["order"] = torch.empty((w.B, w.Nq), dtype=torch.int32, device=dev)
+            b["ws"] = torch.empty(msda.query_order_workspace_bytes(
+                w.B, w.Nq, w.M, w.L, w.P, w.ndim), dtype=torch.uint8, device=dev)
         bufs.append(b)
     stream = torch.cuda.Stream(dev)
-    step, launches_per_step = make_step(msda, w, inp, bufs, stream)
+    step, launches_per_step = make_step(msda, w, inp, bufs, stream, ordered=args.order)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -454,6 +470,8 @@ def run_ours(args):
         "config": {"workload": w.name, "B": w.B, "Nin": w.Nin, "Nq": w.Nq, "M": w.M,
                    "D": w.D, "L": w.L, "P": w.P, "levels": [list(s) for s in w.shapes],
                    "ndim": w.ndim, "pass": "backward" if w.backward else "forward",
+                   "query_order": "computed each step (msda_query_order) and used by the "
+                                  "ordered forward" if args.order else "as given",
                    "samples_per_step_per_gpu": w.samples,
                    "l2": f"cold: {n_sets} rotating input sets of {set_bytes / 1e6:.1f} MB "
                          f"(> 2x L2) between steps",
@@ -465,7 +483,8 @@ def run_ours(args):
                      if peak_src == "measured" else "fallback 6.4 TB/s",
                      "algorithmic_bytes_per_launch": ab["total"],
                      "bytes_breakdown": ab["parts"],
-                     "kernel": "msda fwd" if not w.backward else "zero-fill + msda bwd"},
+                     "kernel": ("zero-fill + msda bwd" if w.backward else
+                                "query order + ordered msda fwd" if args.order else "msda fwd")},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
         "kernel_source_sha256": kernel_source_hash(),
@@ -613,6 +632,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=workloads.names(), default="encoder2d")
+    ap.add_argument("--order", action="store_true",
+                    help="forward workloads: compute the locality-aware query order inside "
+                         "each step and run the ordered forward")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -621,6 +643,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.order and workloads.WORKLOADS[args.workload].backward:
+        ap.error("--order applies to the forward workloads")
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -131,6 +131,50 @@ msda_status msda3d_backward(const msda_dims *dims, const void *value,
                             float *grad_sampling_locations, float *grad_attention_weights,
                             msda_stream_t stream);
 
+/*
+ * Locality-aware query order.  The core's result does not depend on the order in which
+ * queries are processed, but the speed of its gather does: queries whose samples land
+ * close together reuse the same value rows when they run side by side.  This is the
+ * feature-map reuse that "DEFA: Efficient Deformable Attention Acceleration via
+ * Pruning-Assisted Grid-Sampling and Multi-Scale Parallel Processing" (abstract) names
+ * among its memory-access savings, recast as a schedule for a GPU.
+ *
+ * msda_query_order writes query_order[B][Nq] (int32, device memory): for every batch b,
+ * a permutation of 0 .. Nq-1 that sorts the queries by the Morton (Z-order) code of the
+ * mean of their finite sampling locations (all heads, levels and points) on a 64 x 64
+ * (2D) or 16 x 16 x 16 (3D) grid over the normalised square / cube.  Queries with equal
+ * codes come in arbitrary order, which may differ between runs.  Only dims->B, Nq, M, L,
+ * P are used (value_dtype, Nin and D are ignored); ndim is 2 or 3 and
+ * sampling_locations is [B, Nq, M, L, P, ndim] fp32 as for the core.  It needs a
+ * caller-owned device workspace of at least the size msda_query_order_workspace_size
+ * reports (4 * B * (4096 + Nq) bytes plus alignment), 16-byte aligned; its contents on
+ * entry are ignored and on return are unspecified.  Work is enqueued on `stream`.
+ * Nq must be below 2^31.
+ *
+ * msda2d_forward_ordered / msda3d_forward_ordered compute exactly what msda2d_forward /
+ * msda3d_forward compute (bit for bit: every item's arithmetic is unchanged), walking the
+ * queries of batch b in the order query_order[b][0 .. Nq-1].  query_order must be a
+ * permutation of 0 .. Nq-1 per batch (for example from msda_query_order; 4-byte
+ * aligned, device memory).  Entries outside [0, Nq) are clamped into range, which gives
+ * wrong results for the affected queries but never an out-of-range access; a query that
+ * appears twice is computed twice and one that is missing is not written.
+ */
+msda_status msda_query_order_workspace_size(const msda_dims *dims, int32_t ndim, size_t *bytes);
+
+msda_status msda_query_order(const msda_dims *dims, int32_t ndim, const float *sampling_locations,
+                             int32_t *query_order, void *workspace, size_t workspace_bytes,
+                             msda_stream_t stream);
+
+msda_status msda2d_forward_ordered(const msda_dims *dims, const void *value,
+                                   const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                   const float *sampling_locations, const float *attention_weights,
+                                   const int32_t *query_order, void *out, msda_stream_t stream);
+
+msda_status msda3d_forward_ordered(const msda_dims *dims, const void *value,
+                                   const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                   const float *sampling_locations, const float *attention_weights,
+                                   const int32_t *query_order, void *out, msda_stream_t stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none).  The string
  * is owned by the library and stays valid until the next call on the same thread. */
 const char *msda_last_error(void);

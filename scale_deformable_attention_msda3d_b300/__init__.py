@@ -4,6 +4,7 @@ The compute path is libmsda.so (hand-written sm_103a CUDA kernels behind the C A
 ``include/msda.h``); this package is its thin Python binding, with the same names:
 
     msda2d_forward, msda2d_backward, msda3d_forward, msda3d_backward,
+    msda_query_order, msda2d_forward_ordered, msda3d_forward_ordered,
     msda_last_error, msda_abi_version
 
 plus ``MSDeformAttnFunction`` (torch.autograd) for use inside a model.  The library is
@@ -12,8 +13,10 @@ use when missing); without it every call raises -- there is no CPU fallback.
 """
 from ._binding import (EXPORTS, MSDA_BF16, MSDA_ERR_CUDA, MSDA_ERR_INTERNAL,  # noqa: F401
                        MSDA_ERR_INVALID_ARG, MSDA_ERR_UNSUPPORTED, MSDA_F32, MSDA_MAX_LEVELS,
-                       MSDA_MAX_POINTS, MSDA_OK, MsdaError, backward_raw, forward_raw,
-                       library_path, load, make_dims, msda2d_backward, msda2d_forward,
-                       msda3d_backward, msda3d_forward, msda_abi_version, msda_dims,
-                       msda_last_error)
+                       MSDA_MAX_POINTS, MSDA_OK, MsdaError, backward_raw, forward_ordered_raw,
+                       forward_raw, library_path, load, make_dims, msda2d_backward,
+                       msda2d_forward, msda2d_forward_ordered, msda3d_backward,
+                       msda3d_forward, msda3d_forward_ordered, msda_abi_version, msda_dims,
+                       msda_last_error, msda_query_order, query_order_raw,
+                       query_order_workspace_bytes, query_order_workspace_raw)
 from .autograd import MSDeformAttnFunction, ms_deform_attn  # noqa: F401

@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "MSDA_OK", 1: "MSDA_ERR_INVALID_ARG", 2: "MSDA_ERR_UNSUPPORTE
 
 # Every symbol include/msda.h declares.
 EXPORTS = ("msda2d_forward", "msda2d_backward", "msda3d_forward", "msda3d_backward",
-           "msda_last_error", "msda_abi_version")
+           "msda_last_error", "msda_abi_version", "msda_query_order",
+           "msda_query_order_workspace_size", "msda2d_forward_ordered", "msda3d_forward_ordered")
 
 
 class MsdaError(RuntimeError):
@@ -74,6 +75,16 @@ def load(path: Optional[str] = None):
         for name in ("msda2d_backward", "msda3d_backward"):
             getattr(lib, name).argtypes = bwd
             getattr(lib, name).restype = ctypes.c_int
+        fwd_o = [_DIMS_P, _VP, _I64P, _I64P, _VP, _VP, _VP, _VP, _VP]
+        for name in ("msda2d_forward_ordered", "msda3d_forward_ordered"):
+            getattr(lib, name).argtypes = fwd_o
+            getattr(lib, name).restype = ctypes.c_int
+        lib.msda_query_order_workspace_size.argtypes = [_DIMS_P, ctypes.c_int32,
+                                                        ctypes.POINTER(ctypes.c_size_t)]
+        lib.msda_query_order_workspace_size.restype = ctypes.c_int
+        lib.msda_query_order.argtypes = [_DIMS_P, ctypes.c_int32, _VP, _VP, _VP, ctypes.c_size_t,
+                                         _VP]
+        lib.msda_query_order.restype = ctypes.c_int
         lib.msda_last_error.argtypes = []
         lib.msda_last_error.restype = ctypes.c_char_p
         lib.msda_abi_version.argtypes = []
@@ -116,6 +127,34 @@ def forward_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes, level_st
     return fn(ctypes.byref(dims), _VP(value), sh.ctypes.data_as(_I64P),
               ls.ctypes.data_as(_I64P), _VP(sampling_locations), _VP(attention_weights),
               _VP(out), _VP(stream))
+
+
+def forward_ordered_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes,
+                        level_start_index, sampling_locations: int, attention_weights: int,
+                        query_order: int, out: int, stream: int = 0, lib=None) -> int:
+    """Call msda{2,3}d_forward_ordered with raw device pointers; returns the status."""
+    lib = lib or load()
+    sh, ls = _host_i64(spatial_shapes), _host_i64(level_start_index)
+    fn = lib.msda2d_forward_ordered if ndim == 2 else lib.msda3d_forward_ordered
+    return fn(ctypes.byref(dims), _VP(value), sh.ctypes.data_as(_I64P),
+              ls.ctypes.data_as(_I64P), _VP(sampling_locations), _VP(attention_weights),
+              _VP(query_order), _VP(out), _VP(stream))
+
+
+def query_order_workspace_raw(ndim: int, dims: msda_dims, lib=None) -> Tuple[int, int]:
+    """(status, bytes) of msda_query_order_workspace_size."""
+    lib = lib or load()
+    n = ctypes.c_size_t(0)
+    st = lib.msda_query_order_workspace_size(ctypes.byref(dims), int(ndim), ctypes.byref(n))
+    return st, int(n.value)
+
+
+def query_order_raw(ndim: int, dims: msda_dims, sampling_locations: int, query_order: int,
+                    workspace: int, workspace_bytes: int, stream: int = 0, lib=None) -> int:
+    lib = lib or load()
+    return lib.msda_query_order(ctypes.byref(dims), int(ndim), _VP(sampling_locations),
+                                _VP(query_order), _VP(workspace), int(workspace_bytes),
+                                _VP(stream))
 
 
 def backward_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes, level_start_index,
@@ -264,6 +303,84 @@ def msda3d_backward(value, spatial_shapes, level_start_index, sampling_locations
     return _backward(3, value, spatial_shapes, level_start_index, sampling_locations,
                      attention_weights, grad_out, grad_value, grad_sampling_locations,
                      grad_attention_weights, stream)
+
+
+def msda_query_order(sampling_locations, query_order=None, workspace=None, stream=None):
+    """Locality-aware query order: int32 [B, Nq] (device), per batch a permutation of the
+    queries sorted by the Morton code of their mean sampling location.  ``workspace`` (a
+    CUDA uint8 tensor of at least ``query_order_workspace_bytes`` bytes) is allocated when
+    not given."""
+    torch = _torch()
+    loc = sampling_locations
+    _require(loc, "sampling_locations", torch.float32)
+    if loc.dim() != 6 or loc.shape[-1] not in (2, 3):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "sampling_locations must be [B, Nq, M, L, P, 2|3]")
+    ndim = int(loc.shape[-1])
+    B, Nq, M, L, P, _ = loc.shape
+    dims = make_dims(B, 1, Nq, M, 4, L, P, MSDA_F32)
+    lib = load()
+    st, nbytes = query_order_workspace_raw(ndim, dims, lib=lib)
+    _check(lib, st)
+    if query_order is None:
+        query_order = torch.empty((B, Nq), dtype=torch.int32, device=loc.device)
+    _require(query_order, "query_order", torch.int32)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=loc.device)
+    _require(workspace, "workspace")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = query_order_raw(ndim, dims, loc.data_ptr(), query_order.data_ptr(),
+                         workspace.data_ptr(), ws_bytes, _stream_handle(stream, loc.device),
+                         lib=lib)
+    _check(lib, st)
+    return query_order
+
+
+def query_order_workspace_bytes(B, Nq, M, L, P, ndim) -> int:
+    lib = load()
+    st, nbytes = query_order_workspace_raw(ndim, make_dims(B, 1, Nq, M, 4, L, P, MSDA_F32), lib=lib)
+    _check(lib, st)
+    return nbytes
+
+
+def _forward_ordered(ndim, value, spatial_shapes, level_start_index, sampling_locations,
+                     attention_weights, query_order, out=None, stream=None):
+    torch = _torch()
+    dims = _dims_from(value, sampling_locations, ndim)
+    _require(value, "value")
+    _require(sampling_locations, "sampling_locations", torch.float32)
+    _require(attention_weights, "attention_weights", torch.float32)
+    _require(query_order, "query_order", torch.int32)
+    if tuple(attention_weights.shape) != tuple(sampling_locations.shape[:-1]):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "attention_weights must be [B, Nq, M, L, P]")
+    if tuple(query_order.shape) != (dims.B, dims.Nq):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "query_order must be [B, Nq]")
+    if out is None:
+        out = torch.empty((dims.B, dims.Nq, dims.M * dims.D), dtype=value.dtype,
+                          device=value.device)
+    _require(out, "out", value.dtype)
+    if tuple(out.shape) != (dims.B, dims.Nq, dims.M * dims.D):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "out must be [B, Nq, M*D]")
+    lib = load()
+    st = forward_ordered_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
+                             sampling_locations.data_ptr(), attention_weights.data_ptr(),
+                             query_order.data_ptr(), out.data_ptr(),
+                             _stream_handle(stream, value.device), lib=lib)
+    _check(lib, st)
+    return out
+
+
+def msda2d_forward_ordered(value, spatial_shapes, level_start_index, sampling_locations,
+                           attention_weights, query_order, out=None, stream=None):
+    """msda2d_forward walking each batch's queries in ``query_order`` (same result)."""
+    return _forward_ordered(2, value, spatial_shapes, level_start_index, sampling_locations,
+                            attention_weights, query_order, out, stream)
+
+
+def msda3d_forward_ordered(value, spatial_shapes, level_start_index, sampling_locations,
+                           attention_weights, query_order, out=None, stream=None):
+    """msda3d_forward walking each batch's queries in ``query_order`` (same result)."""
+    return _forward_ordered(3, value, spatial_shapes, level_start_index, sampling_locations,
+                            attention_weights, query_order, out, stream)
 
 
 def msda_last_error() -> str:

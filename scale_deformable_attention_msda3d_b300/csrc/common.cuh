@@ -116,6 +116,18 @@ __device__ __forceinline__ float group_sum(float v) {
     return v;
 }
 
+// Work item (b, q, m) at launch position `pos`.  Positions run over (b, i, m); the query
+// is q = order[b * Nq + i] when a query order is given, else i.  Order entries are clamped
+// into [0, Nq), so a malformed order gives wrong results but no out-of-range access.
+__device__ __forceinline__ long long ordered_item(const Params &p, long long pos) {
+    if (p.order == nullptr) return pos;
+    const long long bi = pos / p.M;  // b * Nq + i
+    const long long b = bi / p.Nq;
+    int q = __ldg(p.order + bi);
+    q = q < 0 ? 0 : (q >= p.Nq ? static_cast<int>(p.Nq - 1) : q);
+    return (b * p.Nq + q) * p.M + (pos - bi * p.M);
+}
+
 // ------------------------------------------------------------------ per-sample taps
 
 constexpr unsigned kFull = 0xffffffffu;

@@ -139,7 +139,8 @@ msda_status cuda_status(cudaError_t e, const char *what) {
 
 msda_status forward_impl(int ndim, const msda_dims *dims, const void *value,
                          const int64_t *shapes, const int64_t *level_start, const float *loc,
-                         const float *attn, void *out, msda_stream_t stream) {
+                         const float *attn, const int32_t *order, bool ordered, void *out,
+                         msda_stream_t stream) {
     msda::Params p;
     int G = 0;
     MSDA_TRY(build_params(dims, ndim, shapes, level_start, &p, &G));
@@ -148,10 +149,19 @@ msda_status forward_impl(int ndim, const msda_dims *dims, const void *value,
     MSDA_TRY(check_ptr(loc, "sampling_locations"));
     MSDA_TRY(check_ptr(attn, "attention_weights"));
     MSDA_TRY(check_ptr(out, "out"));
+    if (ordered) {
+        if (!order) return fail(MSDA_ERR_INVALID_ARG, "query_order is NULL");
+        if ((reinterpret_cast<uintptr_t>(order) & 3u) != 0)
+            return fail(MSDA_ERR_INVALID_ARG, "query_order is not 4-byte aligned");
+        if (dims->Nq > INT32_MAX)
+            return fail(MSDA_ERR_UNSUPPORTED, "Nq = %lld: a query order needs Nq < 2^31",
+                        (long long)dims->Nq);
+    }
     p.value = value;
     p.loc = loc;
     p.attn = attn;
     p.out = out;
+    p.order = ordered ? order : nullptr;
     return cuda_status(msda::launch_forward(ndim, dims->value_dtype, G, p,
                                             reinterpret_cast<cudaStream_t>(stream)),
                        "forward launch");
@@ -188,16 +198,92 @@ msda_status backward_impl(int ndim, const msda_dims *dims, const void *value,
                        "backward launch");
 }
 
+// Workspace of msda_query_order: per-batch histogram, then per-query keys (256-byte aligned).
+int64_t order_hist_bytes(int64_t B) { return B * msda::kOrderBuckets * int64_t(sizeof(int)); }
+int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+msda_status order_dims(const msda_dims *d, int ndim, int64_t *bytes) {
+    if (!d) return fail(MSDA_ERR_INVALID_ARG, "dims is NULL");
+    if (ndim != 2 && ndim != 3) return fail(MSDA_ERR_INVALID_ARG, "ndim = %d must be 2 or 3", ndim);
+    if (d->B < 0 || d->Nq < 0)
+        return fail(MSDA_ERR_INVALID_ARG, "B (%lld) and Nq (%lld) must be >= 0",
+                    (long long)d->B, (long long)d->Nq);
+    if (d->M < 1 || d->L < 1 || d->P < 1)
+        return fail(MSDA_ERR_INVALID_ARG, "M, L, P must be >= 1 (got %d %d %d)", d->M, d->L, d->P);
+    if (d->Nq > INT32_MAX) return fail(MSDA_ERR_UNSUPPORTED, "Nq must be below 2^31");
+    int64_t per = 0, t = 0;
+    if (!mul_ok(int64_t(d->M) * d->L, d->P, &per) || !mul_ok(d->B, d->Nq, &t) ||
+        !mul_ok(t, per * ndim * 4, &t) || !mul_ok(d->B, msda::kOrderBuckets * 4, &t) ||
+        per > INT32_MAX)
+        return fail(MSDA_ERR_INVALID_ARG, "sizes overflow");
+    *bytes = align256(order_hist_bytes(d->B)) + align256(d->B * d->Nq * int64_t(sizeof(int)));
+    return MSDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+msda_status msda_query_order_workspace_size(const msda_dims *dims, int32_t ndim, size_t *bytes) {
+    if (!bytes) return fail(MSDA_ERR_INVALID_ARG, "bytes is NULL");
+    int64_t b = 0;
+    MSDA_TRY(order_dims(dims, ndim, &b));
+    *bytes = static_cast<size_t>(b);
+    return MSDA_OK;
+}
+
+msda_status msda_query_order(const msda_dims *dims, int32_t ndim, const float *sampling_locations,
+                             int32_t *query_order, void *workspace, size_t workspace_bytes,
+                             msda_stream_t stream) {
+    int64_t need = 0;
+    MSDA_TRY(order_dims(dims, ndim, &need));
+    if (dims->B == 0 || dims->Nq == 0) return MSDA_OK;
+    MSDA_TRY(check_ptr(sampling_locations, "sampling_locations"));
+    if (!query_order) return fail(MSDA_ERR_INVALID_ARG, "query_order is NULL");
+    if ((reinterpret_cast<uintptr_t>(query_order) & 3u) != 0)
+        return fail(MSDA_ERR_INVALID_ARG, "query_order is not 4-byte aligned");
+    MSDA_TRY(check_ptr(workspace, "workspace"));
+    if (static_cast<int64_t>(workspace_bytes) < need)
+        return fail(MSDA_ERR_INVALID_ARG, "workspace has %zu bytes, %lld needed", workspace_bytes,
+                    (long long)need);
+    msda::Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.B = dims->B;
+    p.Nq = dims->Nq;
+    p.M = dims->M;
+    p.L = dims->L;
+    p.P = dims->P;
+    p.loc = sampling_locations;
+    char *ws = static_cast<char *>(workspace);
+    int *hist = reinterpret_cast<int *>(ws);
+    int *keys = reinterpret_cast<int *>(ws + align256(order_hist_bytes(dims->B)));
+    return cuda_status(msda::launch_query_order(ndim, p, query_order, hist, keys,
+                                                reinterpret_cast<cudaStream_t>(stream)),
+                       "query order launch");
+}
+
+msda_status msda2d_forward_ordered(const msda_dims *dims, const void *value,
+                                   const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                   const float *sampling_locations, const float *attention_weights,
+                                   const int32_t *query_order, void *out, msda_stream_t stream) {
+    return forward_impl(2, dims, value, spatial_shapes, level_start_index, sampling_locations,
+                        attention_weights, query_order, true, out, stream);
+}
+
+msda_status msda3d_forward_ordered(const msda_dims *dims, const void *value,
+                                   const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                   const float *sampling_locations, const float *attention_weights,
+                                   const int32_t *query_order, void *out, msda_stream_t stream) {
+    return forward_impl(3, dims, value, spatial_shapes, level_start_index, sampling_locations,
+                        attention_weights, query_order, true, out, stream);
+}
 
 msda_status msda2d_forward(const msda_dims *dims, const void *value,
                            const int64_t *spatial_shapes, const int64_t *level_start_index,
                            const float *sampling_locations, const float *attention_weights,
                            void *out, msda_stream_t stream) {
     return forward_impl(2, dims, value, spatial_shapes, level_start_index, sampling_locations,
-                        attention_weights, out, stream);
+                        attention_weights, nullptr, false, out, stream);
 }
 
 msda_status msda3d_forward(const msda_dims *dims, const void *value,
@@ -205,7 +291,7 @@ msda_status msda3d_forward(const msda_dims *dims, const void *value,
                            const float *sampling_locations, const float *attention_weights,
                            void *out, msda_stream_t stream) {
     return forward_impl(3, dims, value, spatial_shapes, level_start_index, sampling_locations,
-                        attention_weights, out, stream);
+                        attention_weights, nullptr, false, out, stream);
 }
 
 msda_status msda2d_backward(const msda_dims *dims, const void *value,
@@ -232,6 +318,6 @@ msda_status msda3d_backward(const msda_dims *dims, const void *value,
 
 const char *msda_last_error(void) { return g_err; }
 
-int32_t msda_abi_version(void) { return 10000; }
+int32_t msda_abi_version(void) { return 10100; }
 
 }  // extern "C"

@@ -32,8 +32,8 @@ fwd2d_generic(const __grid_constant__ Params p) {
     const int L = LL > 0 ? LL : p.L;
     const int P = PP > 0 ? PP : p.P;
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const long long item = t / G;
-    if (item >= p.n_items) return;
+    if (t / G >= p.n_items) return;
+    const long long item = ordered_item(p, t / G);
     const int sub = threadIdx.x & (G - 1);
     const int m = static_cast<int>(item % p.M);
     const long long b = item / p.M / p.Nq;
@@ -100,8 +100,8 @@ fwd3d_generic(const __grid_constant__ Params p) {
     const int L = LL > 0 ? LL : p.L;
     const int P = PP > 0 ? PP : p.P;
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const long long item = t / G;
-    if (item >= p.n_items) return;
+    if (t / G >= p.n_items) return;
+    const long long item = ordered_item(p, t / G);
     const int sub = threadIdx.x & (G - 1);
     const int m = static_cast<int>(item % p.M);
     const long long b = item / p.M / p.Nq;
@@ -242,9 +242,10 @@ fwd_tiled(const __grid_constant__ Params p) {
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     // whole warps leave together: the shuffles below need every lane of the warp
     if ((t & ~31LL) / LANES >= p.n_items) return;
-    long long item = t / LANES;
-    const bool active = item < p.n_items;
-    if (!active) item = p.n_items - 1;  // tail lanes redo a real item and store nothing
+    long long pos = t / LANES;
+    const bool active = pos < p.n_items;
+    if (!active) pos = p.n_items - 1;  // tail lanes redo a real item and store nothing
+    const long long item = ordered_item(p, pos);
     const int lane = threadIdx.x & 31;
     const int sub = lane & (G - 1);
     const int sp = SPLIT > 1 ? (lane / G) & (SPLIT - 1) : 0;

@@ -23,6 +23,7 @@ struct Params {
     float *grad_value;          // [B, Nin, M, D]         (backward)
     float *grad_loc;            // like loc               (backward)
     float *grad_attn;           // like attn              (backward)
+    const int *order;           // [B, Nq] query order, or null (forward)
     // sizes
     long long B, Nin, Nq;
     long long n_items;          // B * Nq * M work items (b, q, m)
@@ -44,5 +45,13 @@ struct Params {
 cudaError_t launch_forward(int ndim, int dtype, int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_backward(int ndim, int dtype, int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_zero_fill(float *ptr, long long n_floats, cudaStream_t stream);
+
+// Query order (msda_order.cu): sorts each batch's queries by the Morton code of the mean
+// of their sampling locations.  `hist` holds B * kOrderBuckets ints, `keys` B * Nq ints.
+constexpr int kOrderBits2d = 6;    // bits per axis of the 2D key (64 x 64 cells)
+constexpr int kOrderBits3d = 4;    // bits per axis of the 3D key (16 x 16 x 16 cells)
+constexpr int kOrderBuckets = 1 << 12;
+cudaError_t launch_query_order(int ndim, const Params &p, int *order, int *hist, int *keys,
+                               cudaStream_t stream);
 
 }  // namespace msda

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert msda.msda_abi_version() == 10000
+    assert msda.msda_abi_version() == 10100
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -173,3 +173,40 @@ def test_torch_layer_rejects_host_tensors():
     a = torch.zeros(1, 3, 2, 1, 4)
     with pytest.raises(msda.MsdaError):
         msda.msda2d_forward(v, np.array([[4, 6]]), np.array([0]), loc, a)
+
+
+def test_query_order_workspace_size(lib):
+    st, n = msda.query_order_workspace_raw(2, dims(B=3, Nq=1000))
+    assert st == msda.MSDA_OK
+    # per-batch histogram of 4096 ints, then one int per query, each 256-byte aligned
+    assert n == 3 * 4096 * 4 + ((3 * 1000 * 4 + 255) // 256) * 256
+    assert msda.query_order_workspace_raw(4, dims())[0] == msda.MSDA_ERR_INVALID_ARG
+    assert msda.query_order_workspace_raw(2, dims(P=0))[0] == msda.MSDA_ERR_INVALID_ARG
+    assert msda.query_order_workspace_raw(3, dims(Nq=2 ** 31))[0] == msda.MSDA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(order=0), "query_order is NULL"),
+    (dict(order=FAKE + 2), "4-byte aligned"),
+    (dict(ws=0), "workspace is NULL"),
+    (dict(ws_bytes=1024), "needed"),
+    (dict(loc=FAKE_MIS), "aligned"),
+])
+def test_query_order_rejects_bad_arguments(lib, kw, msg):
+    d = dims()
+    args = dict(loc=FAKE, order=FAKE, ws=FAKE, ws_bytes=1 << 24)
+    args.update(kw)
+    st = msda.query_order_raw(2, d, args["loc"], args["order"], args["ws"], args["ws_bytes"], 0)
+    assert st == msda.MSDA_ERR_INVALID_ARG
+    assert msg in msda.msda_last_error()
+
+
+def test_ordered_forward_rejects_bad_order(lib):
+    for order, msg in ((0, "query_order is NULL"), (FAKE + 1, "4-byte aligned")):
+        st = msda.forward_ordered_raw(2, dims(), FAKE, SH2, LS2, FAKE, FAKE, order, FAKE, 0)
+        assert st == msda.MSDA_ERR_INVALID_ARG and msg in msda.msda_last_error()
+    # the core's own checks still run first
+    st = msda.forward_ordered_raw(2, dims(M=0), FAKE, SH2, LS2, FAKE, FAKE, FAKE, FAKE, 0)
+    assert st == msda.MSDA_ERR_INVALID_ARG
+    # nothing to do: OK without touching the device
+    assert msda.forward_ordered_raw(2, dims(Nq=0), 0, SH2, LS2, 0, 0, 0, 0, 0) == msda.MSDA_OK
