@@ -165,6 +165,25 @@ msda_status msda_query_order(const msda_dims *dims, int32_t ndim, const float *s
                              int32_t *query_order, void *workspace, size_t workspace_bytes,
                              msda_stream_t stream);
 
+/*
+ * msda_query_order without a workspace and without any allocation.  The pages have no
+ * counterpart: this is a service for callers that may not allocate device memory on
+ * their path (a loop that forbids allocation once running, a plugin whose host owns all
+ * device memory, a caller with nowhere to keep a workspace between calls).  The scratch
+ * (per-batch histograms and per-query keys) is a fixed array of about 5 MB inside the
+ * library's device image, present on every GPU that loads the library until the process
+ * exits.  Limits: B <= 64 and B * Nq <= 1048576; larger problems return
+ * MSDA_ERR_UNSUPPORTED (use msda_query_order with a workspace).  The output, arguments
+ * and other errors are those of msda_query_order; no memory is allocated or freed.
+ * The first call on each device looks up that device's copy of the array (make it with
+ * the device current, before capturing any stream on that device).  All calls share the
+ * array: each clears what it needs, but calls whose GPU work overlaps (other streams or
+ * host threads) race on it and may return wrong orders; serialise them.
+ */
+msda_status msda_query_order_static(const msda_dims *dims, int32_t ndim,
+                                    const float *sampling_locations, int32_t *query_order,
+                                    msda_stream_t stream);
+
 msda_status msda2d_forward_ordered(const msda_dims *dims, const void *value,
                                    const int64_t *spatial_shapes, const int64_t *level_start_index,
                                    const float *sampling_locations, const float *attention_weights,

@@ -17,6 +17,6 @@ from ._binding import (EXPORTS, MSDA_BF16, MSDA_ERR_CUDA, MSDA_ERR_INTERNAL,  # 
                        forward_raw, library_path, load, make_dims, msda2d_backward,
                        msda2d_forward, msda2d_forward_ordered, msda3d_backward,
                        msda3d_forward, msda3d_forward_ordered, msda_abi_version, msda_dims,
-                       msda_last_error, msda_query_order, query_order_raw,
+                       msda_last_error, msda_query_order, query_order_raw, query_order_static_raw,
                        query_order_workspace_bytes, query_order_workspace_raw)
 from .autograd import MSDeformAttnFunction, ms_deform_attn  # noqa: F401

@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "MSDA_OK", 1: "MSDA_ERR_INVALID_ARG", 2: "MSDA_ERR_UNSUPPORTE
 # Every symbol include/msda.h declares.
 EXPORTS = ("msda2d_forward", "msda2d_backward", "msda3d_forward", "msda3d_backward",
            "msda_last_error", "msda_abi_version", "msda_query_order",
-           "msda_query_order_workspace_size", "msda2d_forward_ordered", "msda3d_forward_ordered")
+           "msda_query_order_workspace_size", "msda2d_forward_ordered", "msda3d_forward_ordered",
+           "msda_query_order_static")
 
 
 class MsdaError(RuntimeError):
@@ -85,6 +86,8 @@ def load(path: Optional[str] = None):
         lib.msda_query_order.argtypes = [_DIMS_P, ctypes.c_int32, _VP, _VP, _VP, ctypes.c_size_t,
                                          _VP]
         lib.msda_query_order.restype = ctypes.c_int
+        lib.msda_query_order_static.argtypes = [_DIMS_P, ctypes.c_int32, _VP, _VP, _VP]
+        lib.msda_query_order_static.restype = ctypes.c_int
         lib.msda_last_error.argtypes = []
         lib.msda_last_error.restype = ctypes.c_char_p
         lib.msda_abi_version.argtypes = []
@@ -155,6 +158,15 @@ def query_order_raw(ndim: int, dims: msda_dims, sampling_locations: int, query_o
     return lib.msda_query_order(ctypes.byref(dims), int(ndim), _VP(sampling_locations),
                                 _VP(query_order), _VP(workspace), int(workspace_bytes),
                                 _VP(stream))
+
+
+def query_order_static_raw(ndim: int, dims: msda_dims, sampling_locations: int,
+                           query_order: int, stream: int = 0, lib=None) -> int:
+    """msda_query_order_static: the query order with the library's fixed scratch (no
+    workspace, no allocation); returns the status."""
+    lib = lib or load()
+    return lib.msda_query_order_static(ctypes.byref(dims), int(ndim), _VP(sampling_locations),
+                                       _VP(query_order), _VP(stream))
 
 
 def backward_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes, level_start_index,

@@ -262,6 +262,34 @@ msda_status msda_query_order(const msda_dims *dims, int32_t ndim, const float *s
                        "query order launch");
 }
 
+msda_status msda_query_order_static(const msda_dims *dims, int32_t ndim,
+                                    const float *sampling_locations, int32_t *query_order,
+                                    msda_stream_t stream) {
+    int64_t need = 0;
+    MSDA_TRY(order_dims(dims, ndim, &need));
+    if (!msda::static_order_fits(dims->B, dims->Nq))
+        return fail(MSDA_ERR_UNSUPPORTED,
+                    "msda_query_order_static holds at most B = 64 and B * Nq = 1048576 queries "
+                    "(got B = %lld, B * Nq = %lld); use msda_query_order with a workspace",
+                    (long long)dims->B, (long long)(dims->B * dims->Nq));
+    if (dims->B == 0 || dims->Nq == 0) return MSDA_OK;
+    MSDA_TRY(check_ptr(sampling_locations, "sampling_locations"));
+    if (!query_order) return fail(MSDA_ERR_INVALID_ARG, "query_order is NULL");
+    if ((reinterpret_cast<uintptr_t>(query_order) & 3u) != 0)
+        return fail(MSDA_ERR_INVALID_ARG, "query_order is not 4-byte aligned");
+    msda::Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.B = dims->B;
+    p.Nq = dims->Nq;
+    p.M = dims->M;
+    p.L = dims->L;
+    p.P = dims->P;
+    p.loc = sampling_locations;
+    return cuda_status(msda::launch_query_order_static(ndim, p, query_order,
+                                                       reinterpret_cast<cudaStream_t>(stream)),
+                       "query order (fixed scratch) launch");
+}
+
 msda_status msda2d_forward_ordered(const msda_dims *dims, const void *value,
                                    const int64_t *spatial_shapes, const int64_t *level_start_index,
                                    const float *sampling_locations, const float *attention_weights,

@@ -54,4 +54,9 @@ constexpr int kOrderBuckets = 1 << 12;
 cudaError_t launch_query_order(int ndim, const Params &p, int *order, int *hist, int *keys,
                                cudaStream_t stream);
 
+// The same order with its scratch in a fixed device array of the library
+// (msda_order_static.cu); static_order_fits tells whether (B, Nq) fits that array.
+bool static_order_fits(long long B, long long Nq);
+cudaError_t launch_query_order_static(int ndim, const Params &p, int *order, cudaStream_t stream);
+
 }  // namespace msda
