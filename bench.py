@@ -326,11 +326,20 @@ def to_device(inp, w, dev):
     return d
 
 
-def make_step(msda, w, inp, bufs, stream, ordered=False):
+def make_step(msda, w, inp, bufs, stream, ordered=False, prune=0.0):
     """Returns step(i): one pass of the hot path on input set i % len(bufs).  With
     `ordered`, each step first computes the locality-aware query order of its input set
-    (msda_query_order) and then runs the ordered forward, both inside the step."""
+    (msda_query_order) and then runs the ordered forward, both inside the step.  With
+    `prune` > 0 it runs the pruned forward (samples with |A| < prune skipped)."""
     shapes, starts = inp["spatial_shapes"], inp["level_start_index"]
+    if prune > 0:
+        fn = msda.msda2d_forward_pruned if w.ndim == 2 else msda.msda3d_forward_pruned
+
+        def step(i):
+            b = bufs[i % len(bufs)]
+            fn(b["value"], shapes, starts, b["loc"], b["attn"], prune, out=b["out"],
+               stream=stream)
+        return step, 1
     if ordered:
         fn = msda.msda2d_forward_ordered if w.ndim == 2 else msda.msda3d_forward_ordered
 
@@ -413,7 +422,8 @@ def run_ours(args):
                 w.B, w.Nq, w.M, w.L, w.P, w.ndim), dtype=torch.uint8, device=dev)
         bufs.append(b)
     stream = torch.cuda.Stream(dev)
-    step, launches_per_step = make_step(msda, w, inp, bufs, stream, ordered=args.order)
+    step, launches_per_step = make_step(msda, w, inp, bufs, stream, ordered=args.order,
+                                        prune=args.prune)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -472,6 +482,9 @@ def run_ours(args):
                    "ndim": w.ndim, "pass": "backward" if w.backward else "forward",
                    "query_order": "computed each step (msda_query_order) and used by the "
                                   "ordered forward" if args.order else "as given",
+                   "prune": (f"samples with |A| < {args.prune} skipped "
+                             f"({float((np.abs(inp['attention_weights']) < args.prune).mean()):.3f}"
+                             " of them): an approximation") if args.prune > 0 else "none (exact)",
                    "samples_per_step_per_gpu": w.samples,
                    "l2": f"cold: {n_sets} rotating input sets of {set_bytes / 1e6:.1f} MB "
                          f"(> 2x L2) between steps",
@@ -484,7 +497,8 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": ab["total"],
                      "bytes_breakdown": ab["parts"],
                      "kernel": ("zero-fill + msda bwd" if w.backward else
-                                "query order + ordered msda fwd" if args.order else "msda fwd")},
+                                "query order + ordered msda fwd" if args.order else
+                                "pruned msda fwd" if args.prune > 0 else "msda fwd")},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
         "kernel_source_sha256": kernel_source_hash(),
@@ -635,6 +649,9 @@ def main(argv=None):
     ap.add_argument("--order", action="store_true",
                     help="forward workloads: compute the locality-aware query order inside "
                          "each step and run the ordered forward")
+    ap.add_argument("--prune", type=float, default=0.0,
+                    help="forward workloads: skip samples with |A| below this threshold "
+                         "(approximate; 0 = exact)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -643,8 +660,10 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.order and workloads.WORKLOADS[args.workload].backward:
-        ap.error("--order applies to the forward workloads")
+    if (args.order or args.prune > 0) and workloads.WORKLOADS[args.workload].backward:
+        ap.error("--order and --prune apply to the forward workloads")
+    if args.order and args.prune > 0:
+        ap.error("--order and --prune are separate modes")
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)

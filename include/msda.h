@@ -132,6 +132,28 @@ msda_status msda3d_backward(const msda_dims *dims, const void *value,
                             msda_stream_t stream);
 
 /*
+ * Probability-aware pruning of sampling points (an opt-in approximation; "DEFA: Efficient
+ * Deformable Attention Acceleration via Pruning-Assisted Grid-Sampling and Multi-Scale
+ * Parallel Processing", abstract: pruning of sampling points by their probability).
+ * As msda2d_forward / msda3d_forward, except that every sample whose attention weight
+ * has |A| < threshold is skipped: it contributes zero and its corner rows are not read.
+ * threshold = 0 gives exactly the unpruned result.  For every output channel,
+ *   |out_pruned - out| <= sum over skipped samples s of |A_s| * max_c |v_c|
+ * where v_c runs over the in-level corner values of s in that channel (the corner weights
+ * of a sample sum to at most 1).  threshold must be finite and >= 0 (else
+ * MSDA_ERR_INVALID_ARG); all other arguments and errors are those of the forward.
+ */
+msda_status msda2d_forward_pruned(const msda_dims *dims, const void *value,
+                                  const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                  const float *sampling_locations, const float *attention_weights,
+                                  float threshold, void *out, msda_stream_t stream);
+
+msda_status msda3d_forward_pruned(const msda_dims *dims, const void *value,
+                                  const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                  const float *sampling_locations, const float *attention_weights,
+                                  float threshold, void *out, msda_stream_t stream);
+
+/*
  * Locality-aware query order.  The core's result does not depend on the order in which
  * queries are processed, but the speed of its gather does: queries whose samples land
  * close together reuse the same value rows when they run side by side.  This is the

@@ -155,6 +155,57 @@ def msda3d_backward(value, spatial_shapes, level_start_index, sampling_locations
                     attention_weights, grad_out)
 
 
+def forward_pruned(nd: int, value, spatial_shapes, level_start_index, sampling_locations,
+                   attention_weights, threshold: float, lib=None) -> np.ndarray:
+    """The core with probability-aware pruning of sampling points ("DEFA: Efficient
+    Deformable Attention Acceleration via Pruning-Assisted Grid-Sampling and Multi-Scale
+    Parallel Processing", abstract): a sample whose weight has |A| < threshold is dropped
+    from the weighted sum.  A dropped sample contributes exactly nothing, which is what a
+    zero weight contributes to the plain definition (finite values), so the rule is applied
+    to the weights and the plain oracle does the rest."""
+    a = np.asarray(attention_weights, dtype=np.float64)
+    a = np.where(np.abs(a) < threshold, 0.0, a)
+    return forward(nd, value, spatial_shapes, level_start_index, sampling_locations, a,
+                   lib=lib)
+
+
+def pruning_bound(nd: int, value, spatial_shapes, level_start_index, sampling_locations,
+                  attention_weights, threshold: float, lib=None) -> np.ndarray:
+    """Per output channel, the sum over the dropped samples of |A| * max_c |v_c|, v_c the
+    sample's in-level corner values in that channel: an upper bound on |pruned - unpruned|
+    because a sample's corner weights are non-negative and sum to at most 1.  Brute force
+    over every sample and corner (test infrastructure)."""
+    a = np.abs(np.asarray(attention_weights, dtype=np.float64))
+    dropped = np.where(a < threshold, a, 0.0)
+    v = np.abs(np.asarray(value, dtype=np.float64))
+    loc = np.asarray(sampling_locations, dtype=np.float64)
+    shapes = np.asarray(spatial_shapes, dtype=np.int64)
+    starts = np.asarray(level_start_index, dtype=np.int64)
+    B, Nq, M, L, P, _ = loc.shape
+    D = v.shape[-1]
+    bound = np.zeros((B, Nq, M, D))
+    for l in range(L):
+        ext = shapes[l][::-1]                                          # (W, H[, Z])
+        pix = loc[:, :, :, l] * ext - 0.5                              # [B,Nq,M,P,nd]
+        fin = np.all(np.isfinite(pix), axis=-1)
+        i0 = np.floor(np.where(np.isfinite(pix), pix, -5)).astype(np.int64)
+        vmax = np.zeros((B, Nq, M, P, D))
+        for c in range(2 ** nd):
+            idx = i0 + np.array([(c >> k) & 1 for k in range(nd)])
+            inside = fin & np.all((idx >= 0) & (idx < ext), axis=-1)
+            if nd == 2:
+                row = idx[..., 1] * ext[0] + idx[..., 0]
+            else:
+                row = (idx[..., 2] * ext[1] + idx[..., 1]) * ext[0] + idx[..., 0]
+            row = np.where(inside, starts[l] + row, 0)
+            bb = np.arange(B)[:, None, None, None]
+            mm = np.arange(M)[None, None, :, None]
+            vc = v[bb, row, mm]                                        # [B,Nq,M,P,D]
+            vmax = np.maximum(vmax, np.where(inside[..., None], vc, 0.0))
+        bound += (dropped[:, :, :, l, :, None] * vmax).sum(3)
+    return bound.reshape(B, Nq, M * D)
+
+
 def run_inputs(nd: int, inp: Dict[str, np.ndarray], backward_pass: bool = False, lib=None):
     """Convenience: run the oracle on a dict from ``workloads.make_inputs``."""
     args = (inp["value"], inp["spatial_shapes"], inp["level_start_index"],

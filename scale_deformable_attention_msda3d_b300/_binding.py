@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "MSDA_OK", 1: "MSDA_ERR_INVALID_ARG", 2: "MSDA_ERR_UNSUPPORTE
 EXPORTS = ("msda2d_forward", "msda2d_backward", "msda3d_forward", "msda3d_backward",
            "msda_last_error", "msda_abi_version", "msda_query_order",
            "msda_query_order_workspace_size", "msda2d_forward_ordered", "msda3d_forward_ordered",
-           "msda_query_order_static")
+           "msda_query_order_static", "msda2d_forward_pruned", "msda3d_forward_pruned")
 
 
 class MsdaError(RuntimeError):
@@ -86,6 +86,10 @@ def load(path: Optional[str] = None):
         lib.msda_query_order.argtypes = [_DIMS_P, ctypes.c_int32, _VP, _VP, _VP, ctypes.c_size_t,
                                          _VP]
         lib.msda_query_order.restype = ctypes.c_int
+        fwd_p = [_DIMS_P, _VP, _I64P, _I64P, _VP, _VP, ctypes.c_float, _VP, _VP]
+        for name in ("msda2d_forward_pruned", "msda3d_forward_pruned"):
+            getattr(lib, name).argtypes = fwd_p
+            getattr(lib, name).restype = ctypes.c_int
         lib.msda_query_order_static.argtypes = [_DIMS_P, ctypes.c_int32, _VP, _VP, _VP]
         lib.msda_query_order_static.restype = ctypes.c_int
         lib.msda_last_error.argtypes = []
@@ -130,6 +134,18 @@ def forward_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes, level_st
     return fn(ctypes.byref(dims), _VP(value), sh.ctypes.data_as(_I64P),
               ls.ctypes.data_as(_I64P), _VP(sampling_locations), _VP(attention_weights),
               _VP(out), _VP(stream))
+
+
+def forward_pruned_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes,
+                       level_start_index, sampling_locations: int, attention_weights: int,
+                       threshold: float, out: int, stream: int = 0, lib=None) -> int:
+    """Call msda{2,3}d_forward_pruned with raw device pointers; returns the status."""
+    lib = lib or load()
+    sh, ls = _host_i64(spatial_shapes), _host_i64(level_start_index)
+    fn = lib.msda2d_forward_pruned if ndim == 2 else lib.msda3d_forward_pruned
+    return fn(ctypes.byref(dims), _VP(value), sh.ctypes.data_as(_I64P),
+              ls.ctypes.data_as(_I64P), _VP(sampling_locations), _VP(attention_weights),
+              ctypes.c_float(threshold), _VP(out), _VP(stream))
 
 
 def forward_ordered_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes,
@@ -393,6 +409,44 @@ def msda3d_forward_ordered(value, spatial_shapes, level_start_index, sampling_lo
     """msda3d_forward walking each batch's queries in ``query_order`` (same result)."""
     return _forward_ordered(3, value, spatial_shapes, level_start_index, sampling_locations,
                             attention_weights, query_order, out, stream)
+
+
+def _forward_pruned(ndim, value, spatial_shapes, level_start_index, sampling_locations,
+                    attention_weights, threshold, out=None, stream=None):
+    torch = _torch()
+    dims = _dims_from(value, sampling_locations, ndim)
+    _require(value, "value")
+    _require(sampling_locations, "sampling_locations", torch.float32)
+    _require(attention_weights, "attention_weights", torch.float32)
+    if tuple(attention_weights.shape) != tuple(sampling_locations.shape[:-1]):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "attention_weights must be [B, Nq, M, L, P]")
+    if out is None:
+        out = torch.empty((dims.B, dims.Nq, dims.M * dims.D), dtype=value.dtype,
+                          device=value.device)
+    _require(out, "out", value.dtype)
+    if tuple(out.shape) != (dims.B, dims.Nq, dims.M * dims.D):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "out must be [B, Nq, M*D]")
+    lib = load()
+    st = forward_pruned_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
+                            sampling_locations.data_ptr(), attention_weights.data_ptr(),
+                            float(threshold), out.data_ptr(),
+                            _stream_handle(stream, value.device), lib=lib)
+    _check(lib, st)
+    return out
+
+
+def msda2d_forward_pruned(value, spatial_shapes, level_start_index, sampling_locations,
+                          attention_weights, threshold, out=None, stream=None):
+    """msda2d_forward skipping samples with |A| < threshold (opt-in approximation)."""
+    return _forward_pruned(2, value, spatial_shapes, level_start_index, sampling_locations,
+                           attention_weights, threshold, out, stream)
+
+
+def msda3d_forward_pruned(value, spatial_shapes, level_start_index, sampling_locations,
+                          attention_weights, threshold, out=None, stream=None):
+    """msda3d_forward skipping samples with |A| < threshold (opt-in approximation)."""
+    return _forward_pruned(3, value, spatial_shapes, level_start_index, sampling_locations,
+                           attention_weights, threshold, out, stream)
 
 
 def msda_last_error() -> str:

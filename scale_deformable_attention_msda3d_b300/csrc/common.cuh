@@ -132,6 +132,10 @@ __device__ __forceinline__ long long ordered_item(const Params &p, long long pos
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// A sample whose attention weight is below p.prune in magnitude is treated like one that
+// lies outside the level: no corner is valid, nothing is loaded, it contributes zero
+// (probability-aware pruning; p.prune = 0 keeps every sample).
+//
 // Corner data ("taps") of one sample: value row of corner 0 (relative to the item's batch), one
 // validity bit per corner (bit c: corner c lies inside the level) and the corner weights
 // with the attention weight folded in (0 for corners outside).  Corner c has offsets
@@ -146,7 +150,8 @@ __device__ __forceinline__ void make_taps(const Params &p, int l, const float *x
                                           Taps<4> &t, float *frac = nullptr) {
     int x0, y0;
     float fx, fy;
-    const bool ok = pixel_coord(xy[0], p.fW[l], x0, fx) & pixel_coord(xy[1], p.fH[l], y0, fy);
+    const bool ok = pixel_coord(xy[0], p.fW[l], x0, fx) & pixel_coord(xy[1], p.fH[l], y0, fy) &
+                    !(fabsf(a) < p.prune);
     const int W = p.W[l], H = p.H[l];
     const bool vx0 = ok && x0 >= 0, vx1 = ok && x0 < W - 1;
     const bool vy0 = y0 >= 0, vy1 = y0 < H - 1;
@@ -169,7 +174,7 @@ __device__ __forceinline__ void make_taps(const Params &p, int l, const float *x
     int x0, y0, z0;
     float fx, fy, fz;
     const bool ok = pixel_coord(xyz[0], p.fW[l], x0, fx) & pixel_coord(xyz[1], p.fH[l], y0, fy) &
-                    pixel_coord(xyz[2], p.fZ[l], z0, fz);
+                    pixel_coord(xyz[2], p.fZ[l], z0, fz) & !(fabsf(a) < p.prune);
     const int W = p.W[l], H = p.H[l], Z = p.Z[l];
     const bool vx[2] = {ok && x0 >= 0, ok && x0 < W - 1};
     const bool vy[2] = {y0 >= 0, y0 < H - 1};

@@ -1,5 +1,6 @@
 // C ABI of libmsda: host-side validation, parameter packing and dispatch.
 // Nothing is enqueued unless every check passes; no memory is allocated.
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -140,7 +141,7 @@ msda_status cuda_status(cudaError_t e, const char *what) {
 msda_status forward_impl(int ndim, const msda_dims *dims, const void *value,
                          const int64_t *shapes, const int64_t *level_start, const float *loc,
                          const float *attn, const int32_t *order, bool ordered, void *out,
-                         msda_stream_t stream) {
+                         msda_stream_t stream, float prune = 0.f) {
     msda::Params p;
     int G = 0;
     MSDA_TRY(build_params(dims, ndim, shapes, level_start, &p, &G));
@@ -162,6 +163,7 @@ msda_status forward_impl(int ndim, const msda_dims *dims, const void *value,
     p.attn = attn;
     p.out = out;
     p.order = ordered ? order : nullptr;
+    p.prune = prune;
     return cuda_status(msda::launch_forward(ndim, dims->value_dtype, G, p,
                                             reinterpret_cast<cudaStream_t>(stream)),
                        "forward launch");
@@ -288,6 +290,26 @@ msda_status msda_query_order_static(const msda_dims *dims, int32_t ndim,
     return cuda_status(msda::launch_query_order_static(ndim, p, query_order,
                                                        reinterpret_cast<cudaStream_t>(stream)),
                        "query order (fixed scratch) launch");
+}
+
+msda_status msda2d_forward_pruned(const msda_dims *dims, const void *value,
+                                  const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                  const float *sampling_locations, const float *attention_weights,
+                                  float threshold, void *out, msda_stream_t stream) {
+    if (!(threshold >= 0.f) || threshold == INFINITY)
+        return fail(MSDA_ERR_INVALID_ARG, "threshold must be finite and >= 0");
+    return forward_impl(2, dims, value, spatial_shapes, level_start_index, sampling_locations,
+                        attention_weights, nullptr, false, out, stream, threshold);
+}
+
+msda_status msda3d_forward_pruned(const msda_dims *dims, const void *value,
+                                  const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                  const float *sampling_locations, const float *attention_weights,
+                                  float threshold, void *out, msda_stream_t stream) {
+    if (!(threshold >= 0.f) || threshold == INFINITY)
+        return fail(MSDA_ERR_INVALID_ARG, "threshold must be finite and >= 0");
+    return forward_impl(3, dims, value, spatial_shapes, level_start_index, sampling_locations,
+                        attention_weights, nullptr, false, out, stream, threshold);
 }
 
 msda_status msda2d_forward_ordered(const msda_dims *dims, const void *value,

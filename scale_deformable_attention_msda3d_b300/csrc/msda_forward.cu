@@ -60,7 +60,7 @@ fwd2d_generic(const __grid_constant__ Params p) {
             float fx, fy;
             const bool okx = pixel_coord(xy.x, fW, x0, fx);
             const bool oky = pixel_coord(xy.y, fH, y0, fy);
-            const bool ok = okx && oky;
+            const bool ok = okx && oky && !(fabsf(a) < p.prune);
             const bool vx0 = ok && x0 >= 0, vx1 = ok && x0 < W - 1;
             const bool vy0 = y0 >= 0, vy1 = y0 < H - 1;
             const float ay0 = a * (1.f - fy), ay1 = a * fy;
@@ -129,7 +129,7 @@ fwd3d_generic(const __grid_constant__ Params p) {
             int x0, y0, z0;
             float fx, fy, fz;
             const bool ok = pixel_coord(lx, fW, x0, fx) & pixel_coord(ly, fH, y0, fy) &
-                            pixel_coord(lz, fZ, z0, fz);
+                            pixel_coord(lz, fZ, z0, fz) & !(fabsf(a) < p.prune);
             const bool vx[2] = {ok && x0 >= 0, ok && x0 < W - 1};
             const bool vy[2] = {y0 >= 0, y0 < H - 1};
             const bool vz[2] = {z0 >= 0, z0 < Z - 1};

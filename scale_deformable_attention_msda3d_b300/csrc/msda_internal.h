@@ -24,6 +24,7 @@ struct Params {
     float *grad_loc;            // like loc               (backward)
     float *grad_attn;           // like attn              (backward)
     const int *order;           // [B, Nq] query order, or null (forward)
+    float prune;                // forward: samples with |A| < prune are skipped (0: exact)
     // sizes
     long long B, Nin, Nq;
     long long n_items;          // B * Nq * M work items (b, q, m)

@@ -210,3 +210,9 @@ def test_ordered_forward_rejects_bad_order(lib):
     assert st == msda.MSDA_ERR_INVALID_ARG
     # nothing to do: OK without touching the device
     assert msda.forward_ordered_raw(2, dims(Nq=0), 0, SH2, LS2, 0, 0, 0, 0, 0) == msda.MSDA_OK
+
+
+@pytest.mark.parametrize("tau", [-0.1, float("nan"), float("inf")])
+def test_pruned_forward_rejects_bad_threshold(lib, tau):
+    st = msda.forward_pruned_raw(2, dims(), FAKE, SH2, LS2, FAKE, FAKE, tau, FAKE, 0)
+    assert st == msda.MSDA_ERR_INVALID_ARG and "threshold" in msda.msda_last_error()

@@ -82,3 +82,44 @@ def test_adjoint_identities_at_encoder_size(oracle_mod):
     case = {k: inp[k] for k in ("value", "spatial_shapes", "level_start_index",
                                 "sampling_locations", "attention_weights", "grad_out")}
     pins.pin_adjoint_identities(2, case=case)
+
+
+# ---------------------------------------------------------------- probability-aware pruning
+
+def test_pruned_oracle_reduces_to_the_plain_core_and_to_zero(oracle_mod):
+    import workloads
+    for nd, shapes in ((2, [(9, 11), (4, 6)]), (3, [(4, 5, 6), (2, 2, 3)])):
+        inp = workloads.random_problem(nd, shapes, B=2, Nq=30, M=2, D=8, P=4, seed=41,
+                                       backward=False)
+        args = (nd, inp["value"], inp["spatial_shapes"], inp["level_start_index"],
+                inp["sampling_locations"], inp["attention_weights"])
+        plain = oracle_mod.forward(*args)
+        assert np.array_equal(oracle_mod.forward_pruned(*args, 0.0), plain)
+        big = float(np.abs(inp["attention_weights"]).max()) * 2
+        assert np.all(oracle_mod.forward_pruned(*args, big) == 0.0)
+        assert np.all(oracle_mod.pruning_bound(*args, 0.0) == 0.0)
+
+
+def test_pruning_error_stays_within_its_bound_and_the_bound_is_tight(oracle_mod):
+    import workloads
+    inp = workloads.random_problem(2, [(9, 11), (4, 6)], B=2, Nq=50, M=3, D=8, P=4, seed=42,
+                                   backward=False)
+    args = (2, inp["value"], inp["spatial_shapes"], inp["level_start_index"],
+            inp["sampling_locations"], inp["attention_weights"])
+    plain = oracle_mod.forward(*args)
+    for tau in (0.02, 0.05, 0.1):
+        err = np.abs(oracle_mod.forward_pruned(*args, tau) - plain)
+        bound = oracle_mod.pruning_bound(*args, tau)
+        assert np.all(err <= bound + 1e-12)
+        assert bound.max() > 0
+    # tight case: the only dropped sample sits exactly on pixel (3, 3) (corner weights
+    # 1, 0, 0, 0) and that pixel holds the largest value of its cell, so the error equals
+    # the bound
+    H = W = 8
+    value = np.abs(np.random.default_rng(43).standard_normal((1, H * W, 1, 4))) + 0.5
+    value[0, 3 * W + 3] += 10.0
+    loc = np.full((1, 1, 1, 1, 2, 2), (3 + 0.5) / 8)
+    attn = np.array([0.01, 0.99]).reshape(1, 1, 1, 1, 2)
+    a2 = (2, value, np.array([[H, W]]), np.array([0]), loc, attn)
+    err = np.abs(oracle_mod.forward_pruned(*a2, 0.05) - oracle_mod.forward(*a2))
+    assert np.allclose(err, oracle_mod.pruning_bound(*a2, 0.05), rtol=0, atol=1e-15)
