@@ -326,12 +326,31 @@ def to_device(inp, w, dev):
     return d
 
 
-def make_step(msda, w, inp, bufs, stream, ordered=False, prune=0.0):
+def fused_byte_inputs(w, f):
+    """Sampling locations of fused inputs (reference + offset / extent in fp32, as the
+    kernel forms them) for counting the unique value rows; host-side bookkeeping only."""
+    ext = f["spatial_shapes"][:, ::-1].astype(np.float32)
+    loc = (f["reference_points"][:, :, None, :, None, :]
+           + f["sampling_offsets"] / ext[None, None, None, :, None, :])
+    return dict(sampling_locations=loc, spatial_shapes=f["spatial_shapes"],
+                level_start_index=f["level_start_index"],
+                attention_weights=f["attention_logits"])
+
+
+def make_step(msda, w, inp, bufs, stream, ordered=False, prune=0.0, fused=False):
     """Returns step(i): one pass of the hot path on input set i % len(bufs).  With
     `ordered`, each step first computes the locality-aware query order of its input set
     (msda_query_order) and then runs the ordered forward, both inside the step.  With
     `prune` > 0 it runs the pruned forward (samples with |A| < prune skipped)."""
     shapes, starts = inp["spatial_shapes"], inp["level_start_index"]
+    if fused:
+        fn = msda.msda2d_forward_fused if w.ndim == 2 else msda.msda3d_forward_fused
+
+        def step(i):
+            b = bufs[i % len(bufs)]
+            fn(b["value"], shapes, starts, b["ref"], b["loc"], b["attn"], out=b["out"],
+               stream=stream)
+        return step, 1
     if prune > 0:
         fn = msda.msda2d_forward_pruned if w.ndim == 2 else msda.msda3d_forward_pruned
 
@@ -400,8 +419,16 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     msda.load()
     w = workloads.WORKLOADS[args.workload]
-    inp = workloads.make_inputs(w, seed=w.seed + rank)
+    if args.fused:
+        # loc / attn slots carry the offsets and logits; ref the reference points
+        f = workloads.make_fused_inputs(w, seed=w.seed + rank)
+        inp = dict(f, sampling_locations=f["sampling_offsets"],
+                   attention_weights=f["attention_logits"])
+    else:
+        inp = workloads.make_inputs(w, seed=w.seed + rank)
     base = to_device(inp, w, dev)
+    if args.fused:
+        base["ref"] = torch.from_numpy(inp["reference_points"]).to(dev)
     esize = 2 if w.dtype == "bf16" else 4
     set_bytes = sum(t.numel() * t.element_size() for t in base.values())
     set_bytes += w.B * w.Nq * w.M * w.D * esize
@@ -423,7 +450,7 @@ def run_ours(args):
         bufs.append(b)
     stream = torch.cuda.Stream(dev)
     step, launches_per_step = make_step(msda, w, inp, bufs, stream, ordered=args.order,
-                                        prune=args.prune)
+                                        prune=args.prune, fused=args.fused)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -467,7 +494,11 @@ def run_ours(args):
     if rank != 0:
         barrier(world)
         return None
-    ab = algorithmic_bytes(w, inp)
+    ab = algorithmic_bytes(w, fused_byte_inputs(w, inp) if args.fused else inp)
+    if args.fused:
+        ref_b = inp["reference_points"].nbytes
+        ab["total"] += ref_b
+        ab["parts"]["reference_points"] = ref_b
     peak, peak_src = measured_peaks()
     per_launch_s = t_rank / args.steps
     achieved = ab["total"] / per_launch_s / 1e9
@@ -482,6 +513,9 @@ def run_ours(args):
                    "ndim": w.ndim, "pass": "backward" if w.backward else "forward",
                    "query_order": "computed each step (msda_query_order) and used by the "
                                   "ordered forward" if args.order else "as given",
+                   "prologue": ("fused: reference points + pixel offsets + logits in, "
+                                "softmax and locations in the kernel") if args.fused
+                               else "none: locations and weights given",
                    "prune": (f"samples with |A| < {args.prune} skipped "
                              f"({float((np.abs(inp['attention_weights']) < args.prune).mean()):.3f}"
                              " of them): an approximation") if args.prune > 0 else "none (exact)",
@@ -498,7 +532,8 @@ def run_ours(args):
                      "bytes_breakdown": ab["parts"],
                      "kernel": ("zero-fill + msda bwd" if w.backward else
                                 "query order + ordered msda fwd" if args.order else
-                                "pruned msda fwd" if args.prune > 0 else "msda fwd")},
+                                "pruned msda fwd" if args.prune > 0 else
+                                "fused-prologue msda fwd" if args.fused else "msda fwd")},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
         "kernel_source_sha256": kernel_source_hash(),
@@ -649,6 +684,9 @@ def main(argv=None):
     ap.add_argument("--order", action="store_true",
                     help="forward workloads: compute the locality-aware query order inside "
                          "each step and run the ordered forward")
+    ap.add_argument("--fused", action="store_true",
+                    help="forward workloads: reference points, pixel offsets and logits in; "
+                         "the kernel forms locations and the softmax (no e2e leg)")
     ap.add_argument("--prune", type=float, default=0.0,
                     help="forward workloads: skip samples with |A| below this threshold "
                          "(approximate; 0 = exact)")
@@ -662,8 +700,12 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if (args.order or args.prune > 0) and workloads.WORKLOADS[args.workload].backward:
         ap.error("--order and --prune apply to the forward workloads")
-    if args.order and args.prune > 0:
-        ap.error("--order and --prune are separate modes")
+    if sum([bool(args.order), args.prune > 0, bool(args.fused)]) > 1:
+        ap.error("--order, --prune and --fused are separate modes")
+    if args.fused and workloads.WORKLOADS[args.workload].backward:
+        ap.error("--fused applies to the forward workloads")
+    if args.fused:
+        args.no_e2e = True
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -132,6 +132,35 @@ msda_status msda3d_backward(const msda_dims *dims, const void *value,
                             msda_stream_t stream);
 
 /*
+ * Forward with the module's prologue fused in.  The module predicts, per query, sampling
+ * offsets around a reference point and attention logits, and normalises the logits with
+ * a softmax ("Deformable Attention Module": a linear layer gives 3MK channels, 2MK of
+ * offsets and MK logits that a softmax turns into weights; "3D Attention That Knows Where
+ * to Look": reference point plus offsets give the sampling locations; the weights are
+ * blended over all L x P samples).  These calls take those raw pieces and compute
+ *   location[b,q,m,l,p,k] = reference_points[b,q,l,k] + sampling_offsets[b,q,m,l,p,k] / E_lk
+ *   A[b,q,m,:]            = softmax(attention_logits[b,q,m,:]) over the L x P samples
+ * with E_l = (W_l, H_l[, Z_l]) (component k of an offset is in pixels of level l along
+ * W, H, Z), then the core on them, without writing locations or weights to memory.
+ *   reference_points  [B, Nq, L, 2|3]       fp32, normalised (x, y[, z]) per level
+ *   sampling_offsets  [B, Nq, M, L, P, 2|3] fp32, pixels of the sampled level
+ *   attention_logits  [B, Nq, M, L, P]      fp32
+ * The location is formed in fp32 as written (IEEE division, then addition, both
+ * round-to-nearest); the softmax uses the CUDA math library's expf in fp32.  All other
+ * arguments, limits and errors are those of msda2d_forward / msda3d_forward;
+ * reference_points must be non-null and 16-byte aligned.
+ */
+msda_status msda2d_forward_fused(const msda_dims *dims, const void *value,
+                                 const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                 const float *reference_points, const float *sampling_offsets,
+                                 const float *attention_logits, void *out, msda_stream_t stream);
+
+msda_status msda3d_forward_fused(const msda_dims *dims, const void *value,
+                                 const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                 const float *reference_points, const float *sampling_offsets,
+                                 const float *attention_logits, void *out, msda_stream_t stream);
+
+/*
  * Probability-aware pruning of sampling points (an opt-in approximation; "DEFA: Efficient
  * Deformable Attention Acceleration via Pruning-Assisted Grid-Sampling and Multi-Scale
  * Parallel Processing", abstract: pruning of sampling points by their probability).

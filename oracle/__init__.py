@@ -155,6 +155,39 @@ def msda3d_backward(value, spatial_shapes, level_start_index, sampling_locations
                     attention_weights, grad_out)
 
 
+def fused_locations(spatial_shapes, reference_points, sampling_offsets) -> np.ndarray:
+    """Sampling locations of the module's prologue ("3D Attention That Knows Where to
+    Look": reference point plus predicted offsets), in fp32 as an fp32 module forms them:
+    loc[b,q,m,l,p,k] = ref[b,q,l,k] + offset[b,q,m,l,p,k] / E_lk, E_l = (W_l, H_l[, Z_l]),
+    one IEEE division then one IEEE addition."""
+    sh = np.asarray(spatial_shapes, dtype=np.int64)
+    ext = sh[:, ::-1].astype(np.float32)                             # [L, nd] = (W, H[, Z])
+    ref = np.asarray(reference_points, dtype=np.float32)             # [B, Nq, L, nd]
+    off = np.asarray(sampling_offsets, dtype=np.float32)             # [B, Nq, M, L, P, nd]
+    q = off / ext[None, None, None, :, None, :]
+    return ref[:, :, None, :, None, :] + q
+
+
+def softmax_weights(attention_logits) -> np.ndarray:
+    """Attention weights from the logits ("Deformable Attention Module": a softmax over the
+    sampled keys; "3D Attention That Knows Where to Look": one weighted sum over all L x P
+    samples), in double: softmax over the last two axes (L, P) of [B, Nq, M, L, P]."""
+    z = np.asarray(attention_logits, dtype=np.float64)
+    shape = z.shape
+    z = z.reshape(shape[:3] + (-1,))
+    e = np.exp(z - z.max(axis=-1, keepdims=True))
+    return (e / e.sum(axis=-1, keepdims=True)).reshape(shape)
+
+
+def forward_fused(nd: int, value, spatial_shapes, level_start_index, reference_points,
+                  sampling_offsets, attention_logits, lib=None) -> np.ndarray:
+    """The core fed by the module's prologue: locations from reference points and offsets
+    (fp32, as above), weights from a double-precision softmax of the logits."""
+    loc = fused_locations(spatial_shapes, reference_points, sampling_offsets)
+    return forward(nd, value, spatial_shapes, level_start_index, loc,
+                   softmax_weights(attention_logits), lib=lib)
+
+
 def forward_pruned(nd: int, value, spatial_shapes, level_start_index, sampling_locations,
                    attention_weights, threshold: float, lib=None) -> np.ndarray:
     """The core with probability-aware pruning of sampling points ("DEFA: Efficient

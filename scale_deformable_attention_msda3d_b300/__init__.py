@@ -5,7 +5,7 @@ The compute path is libmsda.so (hand-written sm_103a CUDA kernels behind the C A
 
     msda2d_forward, msda2d_backward, msda3d_forward, msda3d_backward,
     msda_query_order, msda2d_forward_ordered, msda3d_forward_ordered,
-    msda2d_forward_pruned, msda3d_forward_pruned,
+    msda2d_forward_pruned, msda3d_forward_pruned, msda2d_forward_fused, msda3d_forward_fused,
     msda_last_error, msda_abi_version
 
 plus ``MSDeformAttnFunction`` (torch.autograd) for use inside a model.  The library is
@@ -16,6 +16,7 @@ from ._binding import (EXPORTS, MSDA_BF16, MSDA_ERR_CUDA, MSDA_ERR_INTERNAL,  # 
                        MSDA_ERR_INVALID_ARG, MSDA_ERR_UNSUPPORTED, MSDA_F32, MSDA_MAX_LEVELS,
                        MSDA_MAX_POINTS, MSDA_OK, MsdaError, backward_raw, forward_ordered_raw,
                        forward_pruned_raw, msda2d_forward_pruned, msda3d_forward_pruned,
+                       forward_fused_raw, msda2d_forward_fused, msda3d_forward_fused,
                        forward_raw, library_path, load, make_dims, msda2d_backward,
                        msda2d_forward, msda2d_forward_ordered, msda3d_backward,
                        msda3d_forward, msda3d_forward_ordered, msda_abi_version, msda_dims,

@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "MSDA_OK", 1: "MSDA_ERR_INVALID_ARG", 2: "MSDA_ERR_UNSUPPORTE
 EXPORTS = ("msda2d_forward", "msda2d_backward", "msda3d_forward", "msda3d_backward",
            "msda_last_error", "msda_abi_version", "msda_query_order",
            "msda_query_order_workspace_size", "msda2d_forward_ordered", "msda3d_forward_ordered",
-           "msda_query_order_static", "msda2d_forward_pruned", "msda3d_forward_pruned")
+           "msda_query_order_static", "msda2d_forward_pruned", "msda3d_forward_pruned",
+           "msda2d_forward_fused", "msda3d_forward_fused")
 
 
 class MsdaError(RuntimeError):
@@ -86,6 +87,9 @@ def load(path: Optional[str] = None):
         lib.msda_query_order.argtypes = [_DIMS_P, ctypes.c_int32, _VP, _VP, _VP, ctypes.c_size_t,
                                          _VP]
         lib.msda_query_order.restype = ctypes.c_int
+        for name in ("msda2d_forward_fused", "msda3d_forward_fused"):
+            getattr(lib, name).argtypes = [_DIMS_P, _VP, _I64P, _I64P, _VP, _VP, _VP, _VP, _VP]
+            getattr(lib, name).restype = ctypes.c_int
         fwd_p = [_DIMS_P, _VP, _I64P, _I64P, _VP, _VP, ctypes.c_float, _VP, _VP]
         for name in ("msda2d_forward_pruned", "msda3d_forward_pruned"):
             getattr(lib, name).argtypes = fwd_p
@@ -134,6 +138,18 @@ def forward_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes, level_st
     return fn(ctypes.byref(dims), _VP(value), sh.ctypes.data_as(_I64P),
               ls.ctypes.data_as(_I64P), _VP(sampling_locations), _VP(attention_weights),
               _VP(out), _VP(stream))
+
+
+def forward_fused_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes,
+                      level_start_index, reference_points: int, sampling_offsets: int,
+                      attention_logits: int, out: int, stream: int = 0, lib=None) -> int:
+    """Call msda{2,3}d_forward_fused with raw device pointers; returns the status."""
+    lib = lib or load()
+    sh, ls = _host_i64(spatial_shapes), _host_i64(level_start_index)
+    fn = lib.msda2d_forward_fused if ndim == 2 else lib.msda3d_forward_fused
+    return fn(ctypes.byref(dims), _VP(value), sh.ctypes.data_as(_I64P),
+              ls.ctypes.data_as(_I64P), _VP(reference_points), _VP(sampling_offsets),
+              _VP(attention_logits), _VP(out), _VP(stream))
 
 
 def forward_pruned_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes,
@@ -433,6 +449,48 @@ def _forward_pruned(ndim, value, spatial_shapes, level_start_index, sampling_loc
                             _stream_handle(stream, value.device), lib=lib)
     _check(lib, st)
     return out
+
+
+def _forward_fused(ndim, value, spatial_shapes, level_start_index, reference_points,
+                   sampling_offsets, attention_logits, out=None, stream=None):
+    torch = _torch()
+    dims = _dims_from(value, sampling_offsets, ndim)
+    _require(value, "value")
+    for t, name in ((reference_points, "reference_points"), (sampling_offsets, "sampling_offsets"),
+                    (attention_logits, "attention_logits")):
+        _require(t, name, torch.float32)
+    if tuple(attention_logits.shape) != tuple(sampling_offsets.shape[:-1]):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "attention_logits must be [B, Nq, M, L, P]")
+    if tuple(reference_points.shape) != (dims.B, dims.Nq, dims.L, ndim):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, f"reference_points must be [B, Nq, L, {ndim}]")
+    if out is None:
+        out = torch.empty((dims.B, dims.Nq, dims.M * dims.D), dtype=value.dtype,
+                          device=value.device)
+    _require(out, "out", value.dtype)
+    if tuple(out.shape) != (dims.B, dims.Nq, dims.M * dims.D):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "out must be [B, Nq, M*D]")
+    lib = load()
+    st = forward_fused_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
+                           reference_points.data_ptr(), sampling_offsets.data_ptr(),
+                           attention_logits.data_ptr(), out.data_ptr(),
+                           _stream_handle(stream, value.device), lib=lib)
+    _check(lib, st)
+    return out
+
+
+def msda2d_forward_fused(value, spatial_shapes, level_start_index, reference_points,
+                         sampling_offsets, attention_logits, out=None, stream=None):
+    """Forward with the prologue fused: location = reference + offset / (W_l, H_l),
+    weights = softmax of the logits over the L*P samples of each query and head."""
+    return _forward_fused(2, value, spatial_shapes, level_start_index, reference_points,
+                          sampling_offsets, attention_logits, out, stream)
+
+
+def msda3d_forward_fused(value, spatial_shapes, level_start_index, reference_points,
+                         sampling_offsets, attention_logits, out=None, stream=None):
+    """3D forward with the prologue fused (offsets in voxels of the sampled level)."""
+    return _forward_fused(3, value, spatial_shapes, level_start_index, reference_points,
+                          sampling_offsets, attention_logits, out, stream)
 
 
 def msda2d_forward_pruned(value, spatial_shapes, level_start_index, sampling_locations,

@@ -128,6 +128,17 @@ __device__ __forceinline__ long long ordered_item(const Params &p, long long pos
     return (b * p.Nq + q) * p.M + (pos - bi * p.M);
 }
 
+// Fused prologue: normalised location of component k of a sample of level l of query
+// (b, q): ref[b, q, l, k] + offset / extent, with IEEE round-to-nearest division and
+// addition (an fp32 module computes the location the same way).
+template <int NDIM>
+__device__ __forceinline__ float fused_location(const Params &p, long long bq, int l, int k,
+                                                float offset) {
+    const float ext = k == 0 ? p.fW[l] : (k == 1 ? p.fH[l] : p.fZ[l]);
+    const float r = __ldg(p.ref + (bq * p.L + l) * NDIM + k);
+    return __fadd_rn(r, __fdiv_rn(offset, ext));
+}
+
 // ------------------------------------------------------------------ per-sample taps
 
 constexpr unsigned kFull = 0xffffffffu;

@@ -141,7 +141,8 @@ msda_status cuda_status(cudaError_t e, const char *what) {
 msda_status forward_impl(int ndim, const msda_dims *dims, const void *value,
                          const int64_t *shapes, const int64_t *level_start, const float *loc,
                          const float *attn, const int32_t *order, bool ordered, void *out,
-                         msda_stream_t stream, float prune = 0.f) {
+                         msda_stream_t stream, float prune = 0.f,
+                         const float *ref = nullptr, bool fused = false) {
     msda::Params p;
     int G = 0;
     MSDA_TRY(build_params(dims, ndim, shapes, level_start, &p, &G));
@@ -162,8 +163,10 @@ msda_status forward_impl(int ndim, const msda_dims *dims, const void *value,
     p.loc = loc;
     p.attn = attn;
     p.out = out;
+    if (fused) MSDA_TRY(check_ptr(ref, "reference_points"));
     p.order = ordered ? order : nullptr;
     p.prune = prune;
+    p.ref = fused ? ref : nullptr;
     return cuda_status(msda::launch_forward(ndim, dims->value_dtype, G, p,
                                             reinterpret_cast<cudaStream_t>(stream)),
                        "forward launch");
@@ -290,6 +293,24 @@ msda_status msda_query_order_static(const msda_dims *dims, int32_t ndim,
     return cuda_status(msda::launch_query_order_static(ndim, p, query_order,
                                                        reinterpret_cast<cudaStream_t>(stream)),
                        "query order (fixed scratch) launch");
+}
+
+msda_status msda2d_forward_fused(const msda_dims *dims, const void *value,
+                                 const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                 const float *reference_points, const float *sampling_offsets,
+                                 const float *attention_logits, void *out, msda_stream_t stream) {
+    return forward_impl(2, dims, value, spatial_shapes, level_start_index, sampling_offsets,
+                        attention_logits, nullptr, false, out, stream, 0.f, reference_points,
+                        true);
+}
+
+msda_status msda3d_forward_fused(const msda_dims *dims, const void *value,
+                                 const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                 const float *reference_points, const float *sampling_offsets,
+                                 const float *attention_logits, void *out, msda_stream_t stream) {
+    return forward_impl(3, dims, value, spatial_shapes, level_start_index, sampling_offsets,
+                        attention_logits, nullptr, false, out, stream, 0.f, reference_points,
+                        true);
 }
 
 msda_status msda2d_forward_pruned(const msda_dims *dims, const void *value,

@@ -9,6 +9,10 @@
 // the level are neither loaded nor weighted.  fp32 accumulation; one store of the item's
 // D channels at the end.
 //
+// With a fused prologue (Params::ref set), `loc` holds per-sample offsets in pixels of the
+// sampled level and `attn` the attention logits: the kernels form location = reference +
+// offset / extent and the softmax of the item's L * P logits themselves.
+//
 // Two kernels:
 // * fwd_tiled (the compiled (L, P) pairs): the locations and weights of an item are read
 //   once with vector loads, spread over the lanes of its group; each lane works out the
@@ -25,7 +29,16 @@ namespace msda {
 
 namespace {
 
-template <int DT, int G, int LL, int PP>
+// Softmax statistics of an item's S logits (fused prologue, generic kernels): max and
+// the sum of expf(z - max).
+__device__ __forceinline__ void logit_stats(const float *z, int S, float &mx, float &sum) {
+    mx = -INFINITY;
+    for (int i = 0; i < S; ++i) mx = fmaxf(mx, __ldg(z + i));
+    sum = 0.f;
+    for (int i = 0; i < S; ++i) sum += expf(__ldg(z + i) - mx);
+}
+
+template <int DT, int G, int LL, int PP, bool FUSED>
 __global__ void __launch_bounds__(256)
 fwd2d_generic(const __grid_constant__ Params p) {
     constexpr int N = Vec<DT>::N;
@@ -42,6 +55,8 @@ fwd2d_generic(const __grid_constant__ Params p) {
                      static_cast<long long>(m) * (rb / p.M) + sub * 16;
     const float2 *lp = reinterpret_cast<const float2 *>(p.loc) + item * L * P;
     const float *ap = p.attn + item * L * P;
+    float zmax = 0.f, zsum = 1.f;
+    if constexpr (FUSED) logit_stats(ap, L * P, zmax, zsum);
 
     float acc[N];
 #pragma unroll
@@ -54,8 +69,14 @@ fwd2d_generic(const __grid_constant__ Params p) {
         const char *vl = vb + static_cast<long long>(p.start[l]) * rb;
 #pragma unroll 4
         for (int k = 0; k < P; ++k) {
-            const float2 xy = __ldg(lp + l * P + k);
-            const float a = __ldg(ap + l * P + k);
+            float2 xy = __ldg(lp + l * P + k);
+            float a = __ldg(ap + l * P + k);
+            if constexpr (FUSED) {
+                const long long bq = item / p.M;
+                xy.x = fused_location<2>(p, bq, l, 0, xy.x);
+                xy.y = fused_location<2>(p, bq, l, 1, xy.y);
+                a = __fdiv_rn(expf(a - zmax), zsum);
+            }
             int x0, y0;
             float fx, fy;
             const bool okx = pixel_coord(xy.x, fW, x0, fx);
@@ -93,7 +114,7 @@ fwd2d_generic(const __grid_constant__ Params p) {
     *reinterpret_cast<uint4 *>(o) = pack(acc);
 }
 
-template <int DT, int G, int LL, int PP>
+template <int DT, int G, int LL, int PP, bool FUSED>
 __global__ void __launch_bounds__(256)
 fwd3d_generic(const __grid_constant__ Params p) {
     constexpr int N = Vec<DT>::N;
@@ -110,6 +131,8 @@ fwd3d_generic(const __grid_constant__ Params p) {
                      static_cast<long long>(m) * (rb / p.M) + sub * 16;
     const float *lp = p.loc + item * L * P * 3;
     const float *ap = p.attn + item * L * P;
+    float zmax = 0.f, zsum = 1.f;
+    if constexpr (FUSED) logit_stats(ap, L * P, zmax, zsum);
 
     float acc[N];
 #pragma unroll
@@ -124,8 +147,15 @@ fwd3d_generic(const __grid_constant__ Params p) {
 #pragma unroll 2
         for (int k = 0; k < P; ++k) {
             const float *xyz = lp + (l * P + k) * 3;
-            const float lx = __ldg(xyz), ly = __ldg(xyz + 1), lz = __ldg(xyz + 2);
-            const float a = __ldg(ap + l * P + k);
+            float lx = __ldg(xyz), ly = __ldg(xyz + 1), lz = __ldg(xyz + 2);
+            float a = __ldg(ap + l * P + k);
+            if constexpr (FUSED) {
+                const long long bq = item / p.M;
+                lx = fused_location<3>(p, bq, l, 0, lx);
+                ly = fused_location<3>(p, bq, l, 1, ly);
+                lz = fused_location<3>(p, bq, l, 2, lz);
+                a = __fdiv_rn(expf(a - zmax), zsum);
+            }
             int x0, y0, z0;
             float fx, fy, fz;
             const bool ok = pixel_coord(lx, fW, x0, fx) & pixel_coord(ly, fH, y0, fy) &
@@ -222,7 +252,8 @@ template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 2, MI
 // Subgroup sp handles samples [sp * SS, (sp + 1) * SS) of the item (sample index
 // l * P + p); its lane `sub` computes the taps of SPL of them.  The corner rows of the
 // next AHEAD samples are loaded before the current sample is summed.
-template <int DT, int G, int VB, int NDIM, int LL, int PP, int SPLIT, int AHEAD, int MINB>
+template <int DT, int G, int VB, int NDIM, int LL, int PP, int SPLIT, int AHEAD, int MINB,
+          bool FUSED>
 __global__ void __launch_bounds__(256, MINB)
 fwd_tiled(const __grid_constant__ Params p) {
     constexpr int N = VB / Vec<DT>::ESIZE;  // channels per lane
@@ -268,6 +299,32 @@ fwd_tiled(const __grid_constant__ Params p) {
 #pragma unroll
             for (int k = 0; k < NDIM; ++k) lv[i * NDIM + k] = have ? __ldcs(lsrc + i * NDIM + k) : 0.f;
             av[i] = have ? __ldcs(asrc + i) : 0.f;
+        }
+    }
+    if constexpr (FUSED) {
+        // prologue: softmax of the item's logits over all its lanes, then the locations
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < SPL; ++i)
+            if (EVEN || sub * SPL + i < SS) mx = fmaxf(mx, av[i]);
+#pragma unroll
+        for (int o = 1; o < LANES; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < SPL; ++i) {
+            av[i] = (EVEN || sub * SPL + i < SS) ? expf(av[i] - mx) : 0.f;
+            sum += av[i];
+        }
+#pragma unroll
+        for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(kFull, sum, o);
+        const long long bq = item / p.M;
+#pragma unroll
+        for (int i = 0; i < SPL; ++i) {
+            av[i] = __fdiv_rn(av[i], sum);
+            const int l = cmin(my0 + i, s0 + SS - 1) / PP;
+#pragma unroll
+            for (int k = 0; k < NDIM; ++k)
+                lv[i * NDIM + k] = fused_location<NDIM>(p, bq, l, k, lv[i * NDIM + k]);
         }
     }
     Taps<NC> tp[SPL];
@@ -353,8 +410,12 @@ cudaError_t launch_tiled(const Params &p, cudaStream_t s) {
     const long long threads = p.n_items * G * SPLIT;
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB>
-        <<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+    if (p.ref)
+        fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, true>
+            <<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+    else
+        fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, false>
+            <<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -384,8 +445,13 @@ cudaError_t forward_nd(const Params &p, cudaStream_t s) {
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>(blocks)), block(256);
-    if constexpr (NDIM == 2) fwd2d_generic<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
-    else fwd3d_generic<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
+    if constexpr (NDIM == 2) {
+        if (p.ref) fwd2d_generic<DT, G, 0, 0, true><<<grid, block, 0, s>>>(p);
+        else fwd2d_generic<DT, G, 0, 0, false><<<grid, block, 0, s>>>(p);
+    } else {
+        if (p.ref) fwd3d_generic<DT, G, 0, 0, true><<<grid, block, 0, s>>>(p);
+        else fwd3d_generic<DT, G, 0, 0, false><<<grid, block, 0, s>>>(p);
+    }
     return cudaGetLastError();
 }
 

@@ -25,6 +25,10 @@ struct Params {
     float *grad_attn;           // like attn              (backward)
     const int *order;           // [B, Nq] query order, or null (forward)
     float prune;                // forward: samples with |A| < prune are skipped (0: exact)
+    // fused prologue (forward): when set, `loc` holds sampling offsets in pixels of the
+    // sampled level and `attn` the attention logits; the location is ref[b, q, l] + offset /
+    // extent and the weights are the softmax of the logits over the item's L * P samples
+    const float *ref;           // [B, Nq, L, NDIM] reference points, or null
     // sizes
     long long B, Nin, Nq;
     long long n_items;          // B * Nq * M work items (b, q, m)

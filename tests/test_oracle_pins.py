@@ -123,3 +123,55 @@ def test_pruning_error_stays_within_its_bound_and_the_bound_is_tight(oracle_mod)
     a2 = (2, value, np.array([[H, W]]), np.array([0]), loc, attn)
     err = np.abs(oracle_mod.forward_pruned(*a2, 0.05) - oracle_mod.forward(*a2))
     assert np.allclose(err, oracle_mod.pruning_bound(*a2, 0.05), rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------- fused prologue
+
+def test_fused_oracle_softmax_and_locations_on_hand_worked_cases(oracle_mod):
+    H, W = 6, 8                                   # not square: a swapped extent shows
+    value = np.random.default_rng(50).standard_normal((1, H * W, 1, 4))
+    sh, ls = np.array([[H, W]]), np.array([0])
+    # reference at the centre of pixel (x=2, y=5); integer pixel offsets (+1, 0) and
+    # (-2, -1) land exactly on pixels (3, 5) and (0, 4): exact gathers of those rows
+    ref = np.array([(2 + 0.5) / W, (5 + 0.5) / H]).reshape(1, 1, 1, 2)
+    off = np.array([[1.0, 0.0], [-2.0, -1.0]]).reshape(1, 1, 1, 1, 2, 2)
+    # logits 0 and ln 3: softmax weights 1/4 and 3/4
+    logits = np.array([0.0, np.log(3.0)]).reshape(1, 1, 1, 1, 2)
+    out = oracle_mod.forward_fused(2, value, sh, ls, ref, off, logits)
+    want = 0.25 * value[0, 5 * W + 3, 0] + 0.75 * value[0, 4 * W + 0, 0]
+    assert np.allclose(out.reshape(-1), want, rtol=0, atol=1e-6)
+    assert np.allclose(oracle_mod.softmax_weights(logits).reshape(-1), [0.25, 0.75],
+                       rtol=0, atol=1e-15)
+    # two levels with one point each: the softmax runs across levels (weights 1/4, 3/4),
+    # and each level's offset is in that level's pixels (level 1 is 3 x 4: pixel (1, 2))
+    sh2 = np.array([[H, W], [3, 4]])
+    ls2 = np.array([0, H * W])
+    v2 = np.random.default_rng(51).standard_normal((1, H * W + 12, 1, 4))
+    ref2 = np.array([[(2 + 0.5) / W, (5 + 0.5) / H], [(0 + 0.5) / 4, (1 + 0.5) / 3]])
+    off2 = np.array([[0.0, 0.0], [1.0, 1.0]]).reshape(1, 1, 1, 2, 1, 2)
+    out2 = oracle_mod.forward_fused(2, v2, sh2, ls2, ref2.reshape(1, 1, 2, 2), off2,
+                                    logits.reshape(1, 1, 1, 2, 1))
+    want2 = 0.25 * v2[0, 5 * W + 2, 0] + 0.75 * v2[0, H * W + 2 * 4 + 1, 0]
+    assert np.allclose(out2.reshape(-1), want2, rtol=0, atol=1e-6)
+
+
+def test_fused_oracle_invariants(oracle_mod):
+    import workloads
+    w = workloads.WORKLOADS["decoder2d"].with_(B=1, Nq=20)
+    f = workloads.make_fused_inputs(w)
+    args = (2, f["value"], f["spatial_shapes"], f["level_start_index"], f["reference_points"],
+            f["sampling_offsets"])
+    base = oracle_mod.forward_fused(*args, f["attention_logits"])
+    # softmax is invariant to a shift of the logits
+    shifted = oracle_mod.forward_fused(*args, f["attention_logits"].astype(np.float64) + 7.0)
+    assert np.allclose(shifted, base, rtol=1e-9, atol=1e-12)
+    # equal logits give uniform weights: a constant value map returns the constant when
+    # every sample lands inside its level (zero offsets at pixel-centre references)
+    const = np.full_like(f["value"], 2.5)
+    inside = (2, const, f["spatial_shapes"], f["level_start_index"],
+              np.full_like(f["reference_points"], 0.5), np.zeros_like(f["sampling_offsets"]))
+    out = oracle_mod.forward_fused(*inside, np.zeros_like(f["attention_logits"]))
+    assert np.allclose(out, 2.5, rtol=0, atol=1e-12)
+    # the weights of every (query, head) sum to one
+    a = oracle_mod.softmax_weights(f["attention_logits"])
+    assert np.allclose(a.reshape(a.shape[:3] + (-1,)).sum(-1), 1.0, atol=1e-12)

@@ -217,6 +217,35 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> Dict[str, np.ndarray
     return out
 
 
+def make_fused_inputs(w: Workload, seed: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """Inputs of the forward with the module's prologue fused in: the value map, per-level
+    reference points [B, Nq, L, ndim] (the query's reference point on every level), offsets
+    [B, Nq, M, L, P, ndim] in pixels of the sampled level (N(0, offset_std_px), or 1 px for
+    a workload that draws its locations directly) and raw logits [B, Nq, M, L, P] ~ N(0,1).
+    Seeded like make_inputs (seed + 7919) but drawn independently of it."""
+    rng = np.random.default_rng((w.seed if seed is None else seed) + 7919)
+    B, Nin, Nq, M, D, L, P, nd = w.B, w.Nin, w.Nq, w.M, w.D, w.L, w.P, w.ndim
+    value32 = rng.standard_normal((B, Nin, M, D), dtype=np.float32)
+    out: Dict[str, np.ndarray] = {}
+    if w.dtype == "bf16":
+        out["value_bits"] = f32_to_bf16_bits(value32)
+        out["value"] = bf16_bits_to_f32(out["value_bits"])
+    else:
+        out["value"] = value32
+    out["spatial_shapes"] = np.array(w.shapes, dtype=np.int64).reshape(L, nd)
+    out["level_start_index"] = level_start_index(w.shapes)
+    if w.query_layout == "uniform_locations":
+        ref = rng.random((B, Nq, nd))
+        std = 1.0
+    else:
+        ref = _reference_points(w, rng)
+        std = w.offset_std_px
+    out["reference_points"] = np.repeat(ref[:, :, None, :], L, axis=2).astype(np.float32)
+    out["sampling_offsets"] = (rng.standard_normal((B, Nq, M, L, P, nd)) * std).astype(np.float32)
+    out["attention_logits"] = rng.standard_normal((B, Nq, M, L, P)).astype(np.float32)
+    return out
+
+
 def out_of_range_fraction(w: Workload, loc: np.ndarray) -> float:
     """Fraction of samples whose location falls outside [0, 1] on some axis."""
     bad = ((loc < 0) | (loc > 1)).any(axis=-1)
