@@ -216,3 +216,15 @@ def test_ordered_forward_rejects_bad_order(lib):
 def test_pruned_forward_rejects_bad_threshold(lib, tau):
     st = msda.forward_pruned_raw(2, dims(), FAKE, SH2, LS2, FAKE, FAKE, tau, FAKE, 0)
     assert st == msda.MSDA_ERR_INVALID_ARG and "threshold" in msda.msda_last_error()
+
+
+def test_fused_forward_rejects_bad_reference_points(lib):
+    for ref, msg in ((0, "reference_points is NULL"), (FAKE_MIS, "reference_points is not")):
+        st = msda.forward_fused_raw(2, dims(), FAKE, SH2, LS2, ref, FAKE, FAKE, FAKE, 0)
+        assert st == msda.MSDA_ERR_INVALID_ARG and msg in msda.msda_last_error()
+    # the core's checks apply to the offsets / logits slots as to locations / weights
+    st = msda.forward_fused_raw(2, dims(), FAKE, SH2, LS2, FAKE, 0, FAKE, FAKE, 0)
+    assert st == msda.MSDA_ERR_INVALID_ARG and "sampling_locations is NULL" in msda.msda_last_error()
+    st = msda.forward_fused_raw(3, dims(Nin=54), FAKE, SH3, LS3, FAKE, FAKE, FAKE, FAKE_MIS, 0)
+    assert st == msda.MSDA_ERR_INVALID_ARG and "out is not 16-byte aligned" in msda.msda_last_error()
+    assert msda.forward_fused_raw(2, dims(Nq=0), 0, SH2, LS2, 0, 0, 0, 0, 0) == msda.MSDA_OK
