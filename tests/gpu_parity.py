@@ -4,7 +4,7 @@ through its binding (the C ABI), run the oracle on the same values, compare.
 Tolerances (written here, used by every GPU test):
   fp32 results: |gpu - ref| <= 1e-5 * max(|ref|, rms(ref), mag) per element, where mag is
                 the magnitude sum of the terms that make up an accumulated gradient entry
-                (standard forward-error scale of a floating-point sum).
+                (the standard forward-error scale of a floating-point sum of those terms).
   bf16 results: |gpu - ref| <= 2e-2 absolute (inputs are unit-scale).
 """
 from __future__ import annotations

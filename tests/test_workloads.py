@@ -5,7 +5,8 @@ import pytest
 import workloads
 
 
-@pytest.mark.parametrize("name", ["tiny2d", "encoder2d", "decoder2d", "encoder2d_bwd"])
+@pytest.mark.parametrize("name", ["tiny2d", "encoder2d", "decoder2d", "encoder2d_bwd",
+                                  "volume3d_bwd"])
 def test_shapes_and_weight_normalisation(name):
     w = workloads.WORKLOADS[name]
     inp = workloads.make_inputs(w)

@@ -25,6 +25,7 @@ method is used at (Deformable DETR's 4-level pyramid, K = 4 points per level):
   decoder2d   B8  L4 (same pyramid)     M8 D32 Nq300    P4  bf16  forward
   volume3d    B1  L4 64^3,32^3,16^3,8^3 M8 D32 Nq32768  P4  bf16  forward
   encoder2d_bwd  encoder2d shapes, fp32, backward with 10% pushed out of range
+  volume3d_bwd   volume3d shapes, bf16 value / grad_out, backward, 10% out of range
 """
 from __future__ import annotations
 
@@ -82,6 +83,9 @@ WORKLOADS: Dict[str, Workload] = {
     "encoder2d_bwd": Workload("encoder2d_bwd", 2, 2, tuple(PYRAMID_2D), 19947, 8, 32,
                               4, "f32", 1004, backward=True, query_layout="per_pixel",
                               offset_std_px=2.0, oob_fraction=0.10),
+    "volume3d_bwd": Workload("volume3d_bwd", 3, 1, tuple(PYRAMID_3D), 32768, 8, 32, 4,
+                             "bf16", 1005, backward=True, query_layout="voxel_centres",
+                             offset_std_px=2.0, oob_fraction=0.10),
 }
 
 
