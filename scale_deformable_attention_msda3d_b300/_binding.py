@@ -260,21 +260,28 @@ def _dims_from(value, sampling_locations, ndim: int) -> msda_dims:
     return make_dims(B, Nin, Nq, M, D, L, P, _dtype_code(value))
 
 
-def _forward(ndim, value, spatial_shapes, level_start_index, sampling_locations,
-             attention_weights, out=None, stream=None):
+def _prepare_forward(ndim, value, sampling_locations, attention_weights, out,
+                     loc_name="sampling_locations", attn_name="attention_weights"):
+    """Checks shared by every forward call; returns (dims, out), allocating out if None."""
     torch = _torch()
     dims = _dims_from(value, sampling_locations, ndim)
     _require(value, "value")
-    _require(sampling_locations, "sampling_locations", torch.float32)
-    _require(attention_weights, "attention_weights", torch.float32)
+    _require(sampling_locations, loc_name, torch.float32)
+    _require(attention_weights, attn_name, torch.float32)
     if tuple(attention_weights.shape) != tuple(sampling_locations.shape[:-1]):
-        raise MsdaError(MSDA_ERR_INVALID_ARG, "attention_weights must be [B, Nq, M, L, P]")
+        raise MsdaError(MSDA_ERR_INVALID_ARG, f"{attn_name} must be [B, Nq, M, L, P]")
     if out is None:
         out = torch.empty((dims.B, dims.Nq, dims.M * dims.D), dtype=value.dtype,
                           device=value.device)
     _require(out, "out", value.dtype)
     if tuple(out.shape) != (dims.B, dims.Nq, dims.M * dims.D):
         raise MsdaError(MSDA_ERR_INVALID_ARG, "out must be [B, Nq, M*D]")
+    return dims, out
+
+
+def _forward(ndim, value, spatial_shapes, level_start_index, sampling_locations,
+             attention_weights, out=None, stream=None):
+    dims, out = _prepare_forward(ndim, value, sampling_locations, attention_weights, out)
     lib = load()
     st = forward_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
                      sampling_locations.data_ptr(), attention_weights.data_ptr(),
@@ -389,21 +396,10 @@ def query_order_workspace_bytes(B, Nq, M, L, P, ndim) -> int:
 def _forward_ordered(ndim, value, spatial_shapes, level_start_index, sampling_locations,
                      attention_weights, query_order, out=None, stream=None):
     torch = _torch()
-    dims = _dims_from(value, sampling_locations, ndim)
-    _require(value, "value")
-    _require(sampling_locations, "sampling_locations", torch.float32)
-    _require(attention_weights, "attention_weights", torch.float32)
+    dims, out = _prepare_forward(ndim, value, sampling_locations, attention_weights, out)
     _require(query_order, "query_order", torch.int32)
-    if tuple(attention_weights.shape) != tuple(sampling_locations.shape[:-1]):
-        raise MsdaError(MSDA_ERR_INVALID_ARG, "attention_weights must be [B, Nq, M, L, P]")
     if tuple(query_order.shape) != (dims.B, dims.Nq):
         raise MsdaError(MSDA_ERR_INVALID_ARG, "query_order must be [B, Nq]")
-    if out is None:
-        out = torch.empty((dims.B, dims.Nq, dims.M * dims.D), dtype=value.dtype,
-                          device=value.device)
-    _require(out, "out", value.dtype)
-    if tuple(out.shape) != (dims.B, dims.Nq, dims.M * dims.D):
-        raise MsdaError(MSDA_ERR_INVALID_ARG, "out must be [B, Nq, M*D]")
     lib = load()
     st = forward_ordered_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
                              sampling_locations.data_ptr(), attention_weights.data_ptr(),
@@ -429,19 +425,7 @@ def msda3d_forward_ordered(value, spatial_shapes, level_start_index, sampling_lo
 
 def _forward_pruned(ndim, value, spatial_shapes, level_start_index, sampling_locations,
                     attention_weights, threshold, out=None, stream=None):
-    torch = _torch()
-    dims = _dims_from(value, sampling_locations, ndim)
-    _require(value, "value")
-    _require(sampling_locations, "sampling_locations", torch.float32)
-    _require(attention_weights, "attention_weights", torch.float32)
-    if tuple(attention_weights.shape) != tuple(sampling_locations.shape[:-1]):
-        raise MsdaError(MSDA_ERR_INVALID_ARG, "attention_weights must be [B, Nq, M, L, P]")
-    if out is None:
-        out = torch.empty((dims.B, dims.Nq, dims.M * dims.D), dtype=value.dtype,
-                          device=value.device)
-    _require(out, "out", value.dtype)
-    if tuple(out.shape) != (dims.B, dims.Nq, dims.M * dims.D):
-        raise MsdaError(MSDA_ERR_INVALID_ARG, "out must be [B, Nq, M*D]")
+    dims, out = _prepare_forward(ndim, value, sampling_locations, attention_weights, out)
     lib = load()
     st = forward_pruned_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
                             sampling_locations.data_ptr(), attention_weights.data_ptr(),
@@ -454,21 +438,11 @@ def _forward_pruned(ndim, value, spatial_shapes, level_start_index, sampling_loc
 def _forward_fused(ndim, value, spatial_shapes, level_start_index, reference_points,
                    sampling_offsets, attention_logits, out=None, stream=None):
     torch = _torch()
-    dims = _dims_from(value, sampling_offsets, ndim)
-    _require(value, "value")
-    for t, name in ((reference_points, "reference_points"), (sampling_offsets, "sampling_offsets"),
-                    (attention_logits, "attention_logits")):
-        _require(t, name, torch.float32)
-    if tuple(attention_logits.shape) != tuple(sampling_offsets.shape[:-1]):
-        raise MsdaError(MSDA_ERR_INVALID_ARG, "attention_logits must be [B, Nq, M, L, P]")
+    dims, out = _prepare_forward(ndim, value, sampling_offsets, attention_logits, out,
+                                 "sampling_offsets", "attention_logits")
+    _require(reference_points, "reference_points", torch.float32)
     if tuple(reference_points.shape) != (dims.B, dims.Nq, dims.L, ndim):
         raise MsdaError(MSDA_ERR_INVALID_ARG, f"reference_points must be [B, Nq, L, {ndim}]")
-    if out is None:
-        out = torch.empty((dims.B, dims.Nq, dims.M * dims.D), dtype=value.dtype,
-                          device=value.device)
-    _require(out, "out", value.dtype)
-    if tuple(out.shape) != (dims.B, dims.Nq, dims.M * dims.D):
-        raise MsdaError(MSDA_ERR_INVALID_ARG, "out must be [B, Nq, M*D]")
     lib = load()
     st = forward_fused_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
                            reference_points.data_ptr(), sampling_offsets.data_ptr(),
