@@ -222,3 +222,21 @@ def test_autograd_wrapper_matches_backward_call(msda):
     check(host(v.grad), rgv, "f32", "autograd grad_value", mag=grad_value_magnitude(2, inp))
     check(host(loc.grad), rgl, "f32", "autograd grad_loc")
     check(host(a.grad), rga, "f32", "autograd grad_attn")
+
+
+def test_autograd_wrapper_3d_bf16(msda):
+    torch = pytest.importorskip("torch")
+    inp = workloads.random_problem(3, SHAPES3, B=1, Nq=30, M=2, D=16, P=4, dtype="bf16",
+                                   seed=18)
+    dev = device_inputs(inp, "bf16")
+    v = dev["value"].clone().requires_grad_(True)
+    loc = dev["sampling_locations"].clone().requires_grad_(True)
+    a = dev["attention_weights"].clone().requires_grad_(True)
+    out = msda.ms_deform_attn(v, inp["spatial_shapes"], inp["level_start_index"], loc, a)
+    check(host(out), oracle.run_inputs(3, inp), "bf16", "autograd 3d forward")
+    (out.float() * dev["grad_out"].float()).sum().backward()
+    rgv, rgl, rga = oracle.run_inputs(3, inp, backward_pass=True)
+    assert v.grad.dtype == torch.bfloat16          # the gradient comes back in value's dtype
+    check(host(v.grad), rgv, "bf16", "autograd 3d grad_value")
+    check(host(loc.grad), rgl, "bf16", "autograd 3d grad_loc")
+    check(host(a.grad), rga, "bf16", "autograd 3d grad_attn")
