@@ -238,15 +238,19 @@ __device__ __forceinline__ uint4 pack16(const float2 *acc) {
 
 // Launch shape of the compiled path for one (ndim, dtype): bytes per lane and row (VB),
 // samples whose corner rows are in flight ahead of the one being summed (AHEAD), and the
-// minimum resident blocks per SM that caps registers (MINB).  Tuned on B300 with the
+// minimum resident blocks of kFwdBlock threads per SM that caps registers (MINB).  Tuned on B300 with the
 // encoder (fp32 2D), decoder (bf16 2D) and volume (bf16 3D) workloads: the gather is bound
 // by how many corner rows are in flight per SM, so occupancy is worth more than depth in
 // 2D, while 3D's 8 corners per sample favour 256-bit loads and a deeper window.
+// Blocks are kFwdBlock = 128 threads: finished work is replaced at a finer grain than with
+// 256 (items take uneven time, e.g. skipped out-of-level corners), worth 6% on the encoder
+// workload.
+constexpr int kFwdBlock = 128;
 template <int NDIM, int DT> struct Shape;
-template <> struct Shape<2, kF32> { static constexpr int VB = 16, AHEAD = 1, MINB = 6; };
-template <> struct Shape<2, kBF16> { static constexpr int VB = 16, AHEAD = 1, MINB = 5; };
-template <> struct Shape<3, kF32> { static constexpr int VB = 32, AHEAD = 2, MINB = 2; };
-template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 2, MINB = 2; };
+template <> struct Shape<2, kF32> { static constexpr int VB = 16, AHEAD = 1, MINB = 12; };
+template <> struct Shape<2, kBF16> { static constexpr int VB = 16, AHEAD = 1, MINB = 10; };
+template <> struct Shape<3, kF32> { static constexpr int VB = 32, AHEAD = 2, MINB = 4; };
+template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 2, MINB = 4; };
 
 // One item = (b, q, m); LANES = G * SPLIT lanes per item; lane = (item, sp, sub).
 // Subgroup sp handles samples [sp * SS, (sp + 1) * SS) of the item (sample index
@@ -254,7 +258,7 @@ template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 2, MI
 // next AHEAD samples are loaded before the current sample is summed.
 template <int DT, int G, int VB, int NDIM, int LL, int PP, int SPLIT, int AHEAD, int MINB,
           bool FUSED>
-__global__ void __launch_bounds__(256, MINB)
+__global__ void __launch_bounds__(kFwdBlock, MINB)
 fwd_tiled(const __grid_constant__ Params p) {
     constexpr int N = VB / Vec<DT>::ESIZE;  // channels per lane
     constexpr int NC = 1 << NDIM;
@@ -408,14 +412,14 @@ template <int DT, int G, int NDIM, int LL, int PP, int SPLIT>
 cudaError_t launch_tiled(const Params &p, cudaStream_t s) {
     using SH = Shape<NDIM, DT>;
     const long long threads = p.n_items * G * SPLIT;
-    const long long blocks = (threads + 255) / 256;
+    const long long blocks = (threads + kFwdBlock - 1) / kFwdBlock;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (p.ref)
         fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, true>
-            <<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+            <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
     else
         fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, false>
-            <<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+            <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
 
