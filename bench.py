@@ -52,20 +52,28 @@ KERNEL_SRC_DIR = os.path.join(ROOT, "scale_deformable_attention_msda3d_b300", "c
 # ----------------------------------------------------------------------------- helpers
 
 
-def kernel_source_hash() -> str:
-    """sha256 over the CUDA / C++ sources of libmsda (identifies the measured kernels)."""
+# Sources that decide what the forward / backward kernels do (shared headers and the ABI
+# layer that packs their parameters, plus the kernel file itself).
+KERNEL_FILES = {
+    "forward": ("common.cuh", "msda_internal.h", "msda_abi.cpp", "msda_forward.cu"),
+    "backward": ("common.cuh", "msda_internal.h", "msda_abi.cpp", "msda_backward.cu"),
+}
+
+
+def kernel_source_hash(kind: str = "forward") -> str:
+    """sha256 over the sources of one kernel family of libmsda (identifies the measured
+    kernels: a profile taken on other sources no longer describes them)."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(KERNEL_SRC_DIR)):
-        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(f.encode())
-            h.update(open(os.path.join(KERNEL_SRC_DIR, f), "rb").read())
+    for f in KERNEL_FILES[kind]:
+        h.update(f.encode())
+        h.update(open(os.path.join(KERNEL_SRC_DIR, f), "rb").read())
     return h.hexdigest()
 
 
 def recorded_traffic(workload: str):
     """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
-    src = kernel_source_hash()
+    taken on the current sources of that kernel family (else None)."""
+    src = kernel_source_hash("backward" if workloads.WORKLOADS[workload].backward else "forward")
     if not os.path.isdir(PROFILE_DIR):
         return None
     for f in sorted(os.listdir(PROFILE_DIR)):
@@ -537,7 +545,7 @@ def run_ours(args):
                                 "fused-prologue msda fwd" if args.fused else "msda fwd")},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
-        "kernel_source_sha256": kernel_source_hash(),
+        "kernel_source_sha256": kernel_source_hash("backward" if w.backward else "forward"),
     }
     if e2e is not None:
         line["e2e"] = e2e

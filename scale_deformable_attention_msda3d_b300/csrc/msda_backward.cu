@@ -361,16 +361,20 @@ bwd_tiled(const __grid_constant__ Params p) {
 
 }
 
-constexpr int kBwdBlock = 256;
+// Block size of the tiled backward: 256 threads in 2D, 128 in 3D (measured on B300: the
+// 3D kernel, 128 registers per thread, ran 17% faster with the finer blocks; 2D ran 2%
+// slower).
+template <int NDIM> constexpr int bwd_block() { return NDIM == 3 ? 128 : 256; }
 
 template <int DT, int G, int NDIM, int LL, int PP>
 cudaError_t launch_bwd_tiled(Params p, cudaStream_t s) {
-    // one round of lane groups per CTA: CTA = (b, m, run of kBwdBlock / G queries)
-    p.qchunk = kBwdBlock / G;
+    constexpr int BT = bwd_block<NDIM>();
+    // one round of lane groups per CTA: CTA = (b, m, run of BT / G queries)
+    p.qchunk = BT / G;
     p.nchunk = static_cast<int>((p.Nq + p.qchunk - 1) / p.qchunk);
     const long long ctas = p.B * p.M * p.nchunk;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    bwd_tiled<DT, G, NDIM, LL, PP, kBwdBlock><<<static_cast<unsigned>(ctas), kBwdBlock, 0, s>>>(p);
+    bwd_tiled<DT, G, NDIM, LL, PP, BT><<<static_cast<unsigned>(ctas), BT, 0, s>>>(p);
     return cudaGetLastError();
 }
 
