@@ -238,10 +238,10 @@ __device__ __forceinline__ uint4 pack16(const float2 *acc) {
 
 // Launch shape of the compiled path for one (ndim, dtype): bytes per lane and row (VB),
 // samples whose corner rows are in flight ahead of the one being summed (AHEAD), and the
-// minimum resident blocks of kFwdBlock threads per SM that caps registers (MINB).  Tuned on B300 with the
-// encoder (fp32 2D), decoder (bf16 2D) and volume (bf16 3D) workloads: the gather is bound
-// by how many corner rows are in flight per SM, so occupancy is worth more than depth in
-// 2D, while 3D's 8 corners per sample favour 256-bit loads and a deeper window.
+// minimum resident blocks of kFwdBlock threads per SM that caps registers (MINB).  Tuned
+// on B300 with the encoder (fp32 2D), decoder (bf16 2D) and volume (bf16 3D) workloads:
+// the gather is bound by how many corner rows are in flight per SM, so occupancy is worth
+// more than depth; 3D's 8 corners per sample favour 256-bit loads.
 // Blocks are kFwdBlock = 128 threads: finished work is replaced at a finer grain than with
 // 256 (items take uneven time, e.g. skipped out-of-level corners), worth 6% on the encoder
 // workload.
@@ -249,8 +249,8 @@ constexpr int kFwdBlock = 128;
 template <int NDIM, int DT> struct Shape;
 template <> struct Shape<2, kF32> { static constexpr int VB = 16, AHEAD = 1, MINB = 12; };
 template <> struct Shape<2, kBF16> { static constexpr int VB = 16, AHEAD = 1, MINB = 10; };
-template <> struct Shape<3, kF32> { static constexpr int VB = 32, AHEAD = 2, MINB = 4; };
-template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 2, MINB = 4; };
+template <> struct Shape<3, kF32> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; };
+template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; };
 
 // One item = (b, q, m); LANES = G * SPLIT lanes per item; lane = (item, sp, sub).
 // Subgroup sp handles samples [sp * SS, (sp + 1) * SS) of the item (sample index
