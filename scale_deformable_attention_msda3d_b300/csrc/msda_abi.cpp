@@ -27,8 +27,8 @@ bool mul_ok(int64_t a, int64_t b, int64_t *r) { return !__builtin_mul_overflow(a
 
 bool misaligned(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; }
 
-// Validates sizes and level metadata and fills the kernel parameters.
-// `need_query_ptrs` is true when there is per-query work (B * Nq > 0).
+// Validates sizes and level metadata and fills the kernel parameters; *G receives the
+// lanes per value row at 16 bytes per lane.
 msda_status build_params(const msda_dims *d, int ndim, const int64_t *shapes,
                          const int64_t *level_start, msda::Params *p, int *G) {
     if (!d) return fail(MSDA_ERR_INVALID_ARG, "dims is NULL");
