@@ -55,18 +55,30 @@ KERNEL_SRC_DIR = os.path.join(ROOT, "scale_deformable_attention_msda3d_b300", "c
 # Sources that decide what the forward / backward kernels do (shared headers and the ABI
 # layer that packs their parameters, plus the kernel file itself).
 KERNEL_FILES = {
-    "forward": ("common.cuh", "msda_internal.h", "msda_abi.cpp", "msda_forward.cu"),
-    "backward": ("common.cuh", "msda_internal.h", "msda_abi.cpp", "msda_backward.cu"),
+    "forward": ("common.cuh", "msda_internal.h", "msda_abi.cpp", "msda_forward.cuh",
+                "msda_forward.cu", "msda_forward_f32_2d.cu", "msda_forward_f32_3d.cu",
+                "msda_forward_bf16_2d.cu", "msda_forward_bf16_3d.cu"),
+    "backward": ("common.cuh", "msda_internal.h", "msda_abi.cpp", "msda_backward.cuh",
+                 "msda_backward.cu", "msda_backward_2d.cu", "msda_backward_3d.cu"),
 }
 
 
+def _code_only(text: str) -> str:
+    """C / C++ / CUDA source with comments and whitespace removed (string literals with
+    comment markers are not expected in these sources)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return re.sub(r"\s+", "", text)
+
+
 def kernel_source_hash(kind: str = "forward") -> str:
-    """sha256 over the sources of one kernel family of libmsda (identifies the measured
-    kernels: a profile taken on other sources no longer describes them)."""
+    """sha256 over the code (comments and whitespace stripped) of one kernel family of
+    libmsda: it identifies the measured kernels, and a profile taken on other code no longer
+    describes them."""
     h = hashlib.sha256()
     for f in KERNEL_FILES[kind]:
         h.update(f.encode())
-        h.update(open(os.path.join(KERNEL_SRC_DIR, f), "rb").read())
+        h.update(_code_only(open(os.path.join(KERNEL_SRC_DIR, f)).read()).encode())
     return h.hexdigest()
 
 

@@ -1,0 +1,10 @@
+// Backward kernels instantiated for 3D, both value dtypes (see msda_backward.cuh).
+#include "msda_backward.cuh"
+
+namespace msda {
+
+cudaError_t launch_backward_3d(int dtype, int G, const Params &p, cudaStream_t s) {
+    return backward_dispatch<3>(dtype, G, p, s);
+}
+
+}  // namespace msda

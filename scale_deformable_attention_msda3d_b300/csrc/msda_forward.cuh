@@ -1,0 +1,484 @@
+// Forward kernels: multi-scale deformable attention sampling + weighted sum.  This header
+// holds the kernel templates; msda_forward_{f32,bf16}_{2d,3d}.cu instantiate them for one
+// value dtype and dimensionality each (so the build compiles them in parallel), and
+// msda_forward.cu dispatches.
+//
+// out[b,q,m,:] = sum_l sum_p A[b,q,m,l,p] * interp_l(value[b, level l, m, :], loc[b,q,m,l,p])
+// ("Deformable Attention Module", DeformAttn equation; multi-scale blending and the 2D->3D
+// changes from "3D Attention That Knows Where to Look").
+//
+// Mapping: a lane group of G lanes per (b, q, m) work item; lane k owns 16 bytes of
+// channels, so a warp-wide 16-byte load brings 32/G whole value rows.  Corners outside
+// the level are neither loaded nor weighted.  fp32 accumulation; one store of the item's
+// D channels at the end.
+//
+// With a fused prologue (Params::ref set), `loc` holds per-sample offsets in pixels of the
+// sampled level and `attn` the attention logits: the kernels form location = reference +
+// offset / extent and the softmax of the item's L * P logits themselves.
+//
+// Two kernels:
+// * fwd_tiled (the compiled (L, P) pairs): the locations and weights of an item are read
+//   once with vector loads, spread over the lanes of its group; each lane works out the
+//   cell, corner validity and weights of its own samples, and the group then walks the
+//   samples in order, taking each sample's corner data from its owner by warp shuffle and
+//   loading the corner rows of the next AHEAD samples before summing the current one.
+//   Optionally the item's samples are split over SPLIT lane groups whose partial sums are
+//   added by shuffles at the end (fewer taps per lane for narrow rows, more loads in flight
+//   when there are few items).  3D uses 32-byte (256-bit) loads per lane.
+// * fwd{2,3}d_generic (any L, P): every lane of the group computes every sample itself.
+#pragma once
+
+#include "common.cuh"
+
+namespace msda {
+
+namespace {
+
+// Softmax statistics of an item's S logits (fused prologue, generic kernels): max and
+// the sum of expf(z - max).
+__device__ __forceinline__ void logit_stats(const float *z, int S, float &mx, float &sum) {
+    mx = -INFINITY;
+    for (int i = 0; i < S; ++i) mx = fmaxf(mx, __ldg(z + i));
+    sum = 0.f;
+    for (int i = 0; i < S; ++i) sum += expf(__ldg(z + i) - mx);
+}
+
+template <int DT, int G, int LL, int PP, bool FUSED>
+__global__ void __launch_bounds__(256)
+fwd2d_generic(const __grid_constant__ Params p) {
+    constexpr int N = Vec<DT>::N;
+    const int L = LL > 0 ? LL : p.L;
+    const int P = PP > 0 ? PP : p.P;
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t / G >= p.n_items) return;
+    const long long item = ordered_item(p, t / G);
+    const int sub = threadIdx.x & (G - 1);
+    const int m = static_cast<int>(item % p.M);
+    const long long b = item / p.M / p.Nq;
+    const long long rb = p.row_bytes;
+    const char *vb = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
+                     static_cast<long long>(m) * (rb / p.M) + sub * 16;
+    const float2 *lp = reinterpret_cast<const float2 *>(p.loc) + item * L * P;
+    const float *ap = p.attn + item * L * P;
+    float zmax = 0.f, zsum = 1.f;
+    if constexpr (FUSED) logit_stats(ap, L * P, zmax, zsum);
+
+    float acc[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) acc[i] = 0.f;
+
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+        const int W = p.W[l], H = p.H[l];
+        const float fW = p.fW[l], fH = p.fH[l];
+        const char *vl = vb + static_cast<long long>(p.start[l]) * rb;
+#pragma unroll 4
+        for (int k = 0; k < P; ++k) {
+            float2 xy = __ldg(lp + l * P + k);
+            float a = __ldg(ap + l * P + k);
+            if constexpr (FUSED) {
+                const long long bq = item / p.M;
+                xy.x = fused_location<2>(p, bq, l, 0, xy.x);
+                xy.y = fused_location<2>(p, bq, l, 1, xy.y);
+                a = __fdiv_rn(expf(a - zmax), zsum);
+            }
+            int x0, y0;
+            float fx, fy;
+            const bool okx = pixel_coord(xy.x, fW, x0, fx);
+            const bool oky = pixel_coord(xy.y, fH, y0, fy);
+            const bool ok = okx && oky && !(fabsf(a) < p.prune);
+            const bool vx0 = ok && x0 >= 0, vx1 = ok && x0 < W - 1;
+            const bool vy0 = y0 >= 0, vy1 = y0 < H - 1;
+            const float ay0 = a * (1.f - fy), ay1 = a * fy;
+            const float w00 = (vy0 && vx0) ? ay0 * (1.f - fx) : 0.f;
+            const float w01 = (vy0 && vx1) ? ay0 * fx : 0.f;
+            const float w10 = (vy1 && vx0) ? ay1 * (1.f - fx) : 0.f;
+            const float w11 = (vy1 && vx1) ? ay1 * fx : 0.f;
+            const char *c00 = vl + static_cast<long long>(y0 * W + x0) * rb;
+            uint4 u00 = make_uint4(0, 0, 0, 0), u01 = u00, u10 = u00, u11 = u00;
+            if (vy0 && vx0) u00 = ldg16(c00);
+            if (vy0 && vx1) u01 = ldg16(c00 + rb);
+            if (vy1 && vx0) u10 = ldg16(c00 + W * rb);
+            if (vy1 && vx1) u11 = ldg16(c00 + (W + 1) * rb);
+            float v[N];
+            unpack(u00, v);
+#pragma unroll
+            for (int i = 0; i < N; ++i) acc[i] = fmaf(w00, v[i], acc[i]);
+            unpack(u01, v);
+#pragma unroll
+            for (int i = 0; i < N; ++i) acc[i] = fmaf(w01, v[i], acc[i]);
+            unpack(u10, v);
+#pragma unroll
+            for (int i = 0; i < N; ++i) acc[i] = fmaf(w10, v[i], acc[i]);
+            unpack(u11, v);
+#pragma unroll
+            for (int i = 0; i < N; ++i) acc[i] = fmaf(w11, v[i], acc[i]);
+        }
+    }
+    char *o = static_cast<char *>(p.out) + item * (rb / p.M) + sub * 16;
+    *reinterpret_cast<uint4 *>(o) = pack(acc);
+}
+
+template <int DT, int G, int LL, int PP, bool FUSED>
+__global__ void __launch_bounds__(256)
+fwd3d_generic(const __grid_constant__ Params p) {
+    constexpr int N = Vec<DT>::N;
+    const int L = LL > 0 ? LL : p.L;
+    const int P = PP > 0 ? PP : p.P;
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t / G >= p.n_items) return;
+    const long long item = ordered_item(p, t / G);
+    const int sub = threadIdx.x & (G - 1);
+    const int m = static_cast<int>(item % p.M);
+    const long long b = item / p.M / p.Nq;
+    const long long rb = p.row_bytes;
+    const char *vb = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
+                     static_cast<long long>(m) * (rb / p.M) + sub * 16;
+    const float *lp = p.loc + item * L * P * 3;
+    const float *ap = p.attn + item * L * P;
+    float zmax = 0.f, zsum = 1.f;
+    if constexpr (FUSED) logit_stats(ap, L * P, zmax, zsum);
+
+    float acc[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) acc[i] = 0.f;
+
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+        const int W = p.W[l], H = p.H[l], Z = p.Z[l];
+        const float fW = p.fW[l], fH = p.fH[l], fZ = p.fZ[l];
+        const char *vl = vb + static_cast<long long>(p.start[l]) * rb;
+        const long long sy = W * rb, sz = static_cast<long long>(H) * W * rb;
+#pragma unroll 2
+        for (int k = 0; k < P; ++k) {
+            const float *xyz = lp + (l * P + k) * 3;
+            float lx = __ldg(xyz), ly = __ldg(xyz + 1), lz = __ldg(xyz + 2);
+            float a = __ldg(ap + l * P + k);
+            if constexpr (FUSED) {
+                const long long bq = item / p.M;
+                lx = fused_location<3>(p, bq, l, 0, lx);
+                ly = fused_location<3>(p, bq, l, 1, ly);
+                lz = fused_location<3>(p, bq, l, 2, lz);
+                a = __fdiv_rn(expf(a - zmax), zsum);
+            }
+            int x0, y0, z0;
+            float fx, fy, fz;
+            const bool ok = pixel_coord(lx, fW, x0, fx) & pixel_coord(ly, fH, y0, fy) &
+                            pixel_coord(lz, fZ, z0, fz) & !(fabsf(a) < p.prune);
+            const bool vx[2] = {ok && x0 >= 0, ok && x0 < W - 1};
+            const bool vy[2] = {y0 >= 0, y0 < H - 1};
+            const bool vz[2] = {z0 >= 0, z0 < Z - 1};
+            const float wx[2] = {1.f - fx, fx};
+            const float wy[2] = {1.f - fy, fy};
+            const float wz[2] = {a * (1.f - fz), a * fz};
+            const char *c000 = vl + static_cast<long long>((z0 * H + y0) * W + x0) * rb;
+            uint4 u[8];
+            float w[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
+                const bool inside = vx[dx] && vy[dy] && vz[dz];
+                w[c] = inside ? wz[dz] * wy[dy] * wx[dx] : 0.f;
+                u[c] = make_uint4(0, 0, 0, 0);
+                if (inside) u[c] = ldg16(c000 + dz * sz + dy * sy + dx * rb);
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float v[N];
+                unpack(u[c], v);
+#pragma unroll
+                for (int i = 0; i < N; ++i) acc[i] = fmaf(w[c], v[i], acc[i]);
+            }
+        }
+    }
+    char *o = static_cast<char *>(p.out) + item * (rb / p.M) + sub * 16;
+    *reinterpret_cast<uint4 *>(o) = pack(acc);
+}
+
+
+// ------------------------------------------------------------------ compiled (L, P)
+
+// VB bytes of one value row held by one lane (16: one 128-bit load; 32: one 256-bit load).
+template <int VB> struct Slice;
+template <> struct Slice<16> { uint4 a; };
+template <> struct Slice<32> { uint4 a, b; };
+
+__device__ __forceinline__ void load_slice(const char *p, Slice<16> &r) { r.a = ldg16(p); }
+__device__ __forceinline__ void load_slice(const char *p, Slice<32> &r) { ldg32(p, r.a, r.b); }
+__device__ __forceinline__ void zero_slice(Slice<16> &r) { r.a = make_uint4(0, 0, 0, 0); }
+__device__ __forceinline__ void zero_slice(Slice<32> &r) {
+    r.a = make_uint4(0, 0, 0, 0);
+    r.b = r.a;
+}
+
+// acc += w * (the channels of one 16-byte piece), packed fp32x2 FMAs (same rounding as fmaf).
+template <int DT>
+__device__ __forceinline__ void fma16(float2 *acc, float w, const uint4 &u) {
+    constexpr int NV = Vec<DT>::N;
+    float v[NV];
+    unpack(u, v);
+    const float2 w2 = make_float2(w, w);
+#pragma unroll
+    for (int i = 0; i < NV / 2; ++i) acc[i] = __ffma2_rn(w2, make_float2(v[2 * i], v[2 * i + 1]), acc[i]);
+}
+
+template <int DT, int VB>
+__device__ __forceinline__ void fma_slice(float2 *acc, float w, const Slice<VB> &r) {
+    fma16<DT>(acc, w, r.a);
+    if constexpr (VB == 32) fma16<DT>(acc + Vec<DT>::N / 2, w, r.b);
+}
+
+// 16 bytes of output channels from acc[half * NV/2 ...] (bf16: one RNE rounding).
+template <int DT>
+__device__ __forceinline__ uint4 pack16(const float2 *acc) {
+    constexpr int NV = Vec<DT>::N;
+    float r[NV];
+#pragma unroll
+    for (int i = 0; i < NV / 2; ++i) {
+        r[2 * i] = acc[i].x;
+        r[2 * i + 1] = acc[i].y;
+    }
+    return pack(r);
+}
+
+// Launch shape of the compiled path for one (ndim, dtype): bytes per lane and row (VB),
+// samples whose corner rows are in flight ahead of the one being summed (AHEAD), and the
+// minimum resident blocks of kFwdBlock threads per SM that caps registers (MINB).  Tuned
+// on B300 with the encoder (fp32 2D), decoder (bf16 2D) and volume (bf16 3D) workloads:
+// the gather is bound by how many corner rows are in flight per SM, so occupancy is worth
+// more than depth; 3D's 8 corners per sample favour 256-bit loads.
+// Blocks are kFwdBlock = 128 threads: finished work is replaced at a finer grain than with
+// 256 (items take uneven time, e.g. skipped out-of-level corners), worth 6% on the encoder
+// workload.
+constexpr int kFwdBlock = 128;
+template <int NDIM, int DT> struct Shape;
+template <> struct Shape<2, kF32> { static constexpr int VB = 16, AHEAD = 1, MINB = 12; };
+template <> struct Shape<2, kBF16> { static constexpr int VB = 16, AHEAD = 1, MINB = 10; };
+template <> struct Shape<3, kF32> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; };
+template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; };
+
+// One item = (b, q, m); LANES = G * SPLIT lanes per item; lane = (item, sp, sub).
+// Subgroup sp handles samples [sp * SS, (sp + 1) * SS) of the item (sample index
+// l * P + p); its lane `sub` computes the taps of SPL of them.  The corner rows of the
+// next AHEAD samples are loaded before the current sample is summed.
+template <int DT, int G, int VB, int NDIM, int LL, int PP, int SPLIT, int AHEAD, int MINB,
+          bool FUSED>
+__global__ void __launch_bounds__(kFwdBlock, MINB)
+fwd_tiled(const __grid_constant__ Params p) {
+    constexpr int N = VB / Vec<DT>::ESIZE;  // channels per lane
+    constexpr int NC = 1 << NDIM;
+    constexpr int S = LL * PP;
+    static_assert(S % SPLIT == 0, "SPLIT must divide L * P");
+    constexpr int SS = S / SPLIT;
+    constexpr int SPL = (SS + G - 1) / G;
+    constexpr int LANES = G * SPLIT;
+    static_assert(LANES <= 32 && (32 % LANES) == 0, "lanes per item must divide the warp");
+    // when every lane owns exactly SPL samples, read them with vector loads
+    constexpr bool EVEN = (SS % G) == 0;
+    constexpr int ALOC = cmin(cmin(falign(S * NDIM), falign(SS * NDIM)), falign(SPL * NDIM));
+    constexpr int AATT = cmin(cmin(falign(S), falign(SS)), falign(SPL));
+    constexpr int DEPTH = AHEAD + 1;
+
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    // whole warps leave together: the shuffles below need every lane of the warp
+    if ((t & ~31LL) / LANES >= p.n_items) return;
+    long long pos = t / LANES;
+    const bool active = pos < p.n_items;
+    if (!active) pos = p.n_items - 1;  // tail lanes redo a real item and store nothing
+    const long long item = ordered_item(p, pos);
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & (G - 1);
+    const int sp = SPLIT > 1 ? (lane / G) & (SPLIT - 1) : 0;
+    const int m = static_cast<int>(item % p.M);
+    const long long b = item / p.M / p.Nq;
+    const int s0 = sp * SS;                  // first sample of this subgroup
+    const int my0 = s0 + sub * SPL;          // first sample whose taps this lane computes
+
+    // 1. locations and weights of this lane's samples, then their taps
+    float lv[SPL * NDIM], av[SPL];
+    const float *lsrc = p.loc + (item * S + my0) * NDIM;
+    const float *asrc = p.attn + item * S + my0;
+    if constexpr (EVEN) {
+        load_stream<SPL * NDIM, ALOC>(lsrc, lv);
+        load_stream<SPL, AATT>(asrc, av);
+    } else {
+#pragma unroll
+        for (int i = 0; i < SPL; ++i) {
+            const bool have = sub * SPL + i < SS;
+#pragma unroll
+            for (int k = 0; k < NDIM; ++k) lv[i * NDIM + k] = have ? __ldcs(lsrc + i * NDIM + k) : 0.f;
+            av[i] = have ? __ldcs(asrc + i) : 0.f;
+        }
+    }
+    if constexpr (FUSED) {
+        // prologue: softmax of the item's logits over all its lanes, then the locations
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < SPL; ++i)
+            if (EVEN || sub * SPL + i < SS) mx = fmaxf(mx, av[i]);
+#pragma unroll
+        for (int o = 1; o < LANES; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < SPL; ++i) {
+            av[i] = (EVEN || sub * SPL + i < SS) ? expf(av[i] - mx) : 0.f;
+            sum += av[i];
+        }
+#pragma unroll
+        for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(kFull, sum, o);
+        const long long bq = item / p.M;
+#pragma unroll
+        for (int i = 0; i < SPL; ++i) {
+            av[i] = __fdiv_rn(av[i], sum);
+            const int l = cmin(my0 + i, s0 + SS - 1) / PP;
+#pragma unroll
+            for (int k = 0; k < NDIM; ++k)
+                lv[i * NDIM + k] = fused_location<NDIM>(p, bq, l, k, lv[i * NDIM + k]);
+        }
+    }
+    Taps<NC> tp[SPL];
+#pragma unroll
+    for (int i = 0; i < SPL; ++i) {
+        // a lane past the end of the subgroup's samples computes a harmless copy of
+        // sample my0 clamped into range (never shuffled out)
+        const int j = cmin(my0 + i, s0 + SS - 1);
+        make_taps(p, j / PP, lv + i * NDIM, av[i], tp[i]);
+    }
+
+    // 2. walk the subgroup's samples; corner rows are VB-byte slices per lane
+    const long long rb = p.row_bytes;
+    const char *vb = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
+                     static_cast<long long>(m) * (rb / p.M) + sub * VB;
+    float2 acc[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) acc[i] = make_float2(0.f, 0.f);
+
+    Taps<NC> tq[DEPTH];
+    Slice<VB> u[DEPTH][NC];
+    // taps of sample s from its owner lane, and its in-level corner rows
+    auto fetch = [&](int s, int slot) {
+        tq[slot] = shfl_taps(tp[s % SPL], s / SPL, G);
+        const int l = (s0 + s) / PP;  // a constant when SPLIT == 1
+        const char *c0 = vb + static_cast<long long>(tq[slot].row) * p.rb32;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
+            long long off = dx ? rb : 0;
+            if (dy) off += p.sy[l];
+            if (dz) off += p.sz[l];
+            zero_slice(u[slot][c]);
+            if (tq[slot].ok & (1u << c)) load_slice(c0 + off, u[slot][c]);
+        }
+    };
+#pragma unroll
+    for (int k = 0; k < AHEAD; ++k)
+        if (k < SS) fetch(k, k);
+#pragma unroll
+    for (int s = 0; s < SS; ++s) {
+        if (s + AHEAD < SS) fetch(s + AHEAD, (s + AHEAD) % DEPTH);
+        const int slot = s % DEPTH;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) fma_slice<DT, VB>(acc, tq[slot].w[c], u[slot][c]);
+    }
+
+    // 3. add the subgroups' partial sums, store the item's channels
+    if constexpr (SPLIT > 1) {
+#pragma unroll
+        for (int o = G; o < LANES; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                acc[i].x += __shfl_xor_sync(kFull, acc[i].x, o);
+                acc[i].y += __shfl_xor_sync(kFull, acc[i].y, o);
+            }
+    }
+    if (active && sp == 0) {
+        uint4 *o = reinterpret_cast<uint4 *>(static_cast<char *>(p.out) + item * (rb / p.M) + sub * VB);
+        __stcs(o, pack16<DT>(acc));
+        if constexpr (VB == 32) __stcs(o + 1, pack16<DT>(acc + Vec<DT>::N / 2));
+    }
+}
+
+// Lane groups per item for the compiled path.  Narrow rows (few lanes per row) split an
+// item's samples until one lane computes the taps of at most MAX_SPL samples (their
+// registers would spill otherwise); then the split grows while the launch would leave the
+// GPU short of resident warps.
+template <int G, int S, int NDIM>
+int pick_split(long long n_items) {
+    constexpr int MAX_SPL = NDIM == 2 ? 4 : 2;
+    constexpr long long kWantThreads = 148LL * 2048 * 2;  // two full waves of the B300's SMs
+    auto can_double = [](int split) { return split < 4 && G * split * 2 <= 32 && S % (split * 2) == 0; };
+    int split = 1;
+    while (can_double(split) && S / split > MAX_SPL * G) split *= 2;
+    while (can_double(split) && n_items * G * split < kWantThreads) split *= 2;
+    return split;
+}
+
+template <int DT, int G, int NDIM, int LL, int PP, int SPLIT>
+cudaError_t launch_tiled(const Params &p, cudaStream_t s) {
+    using SH = Shape<NDIM, DT>;
+    const long long threads = p.n_items * G * SPLIT;
+    const long long blocks = (threads + kFwdBlock - 1) / kFwdBlock;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (p.ref)
+        fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, true>
+            <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
+    else
+        fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, false>
+            <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+// G16 = lanes per row at 16 bytes per lane; the kernel uses G = row bytes / VB lanes.
+template <int DT, int G16, int NDIM, int LL, int PP>
+cudaError_t launch_tiled_split(const Params &p, cudaStream_t s) {
+    constexpr int VB = Shape<NDIM, DT>::VB;
+    constexpr int G = G16 * 16 / VB;
+    static_assert(G >= 1, "rows narrower than one lane's slice take the generic path");
+    const int split = pick_split<G, LL * PP, NDIM>(p.n_items);
+    if constexpr (G <= 16) {
+        if (split == 2) return launch_tiled<DT, G, NDIM, LL, PP, 2>(p, s);
+    }
+    if constexpr (G <= 8) {
+        if (split == 4) return launch_tiled<DT, G, NDIM, LL, PP, 4>(p, s);
+    }
+    return launch_tiled<DT, G, NDIM, LL, PP, 1>(p, s);
+}
+
+template <int DT, int G, int NDIM>
+cudaError_t forward_nd(const Params &p, cudaStream_t s) {
+    if constexpr (G * 16 >= Shape<NDIM, DT>::VB) {
+        if (p.L == 4 && p.P == 4) return launch_tiled_split<DT, G, NDIM, 4, 4>(p, s);
+        if (p.L == 1 && p.P == 4) return launch_tiled_split<DT, G, NDIM, 1, 4>(p, s);
+    }
+    const long long threads = p.n_items * G;
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(blocks)), block(256);
+    if constexpr (NDIM == 2) {
+        if (p.ref) fwd2d_generic<DT, G, 0, 0, true><<<grid, block, 0, s>>>(p);
+        else fwd2d_generic<DT, G, 0, 0, false><<<grid, block, 0, s>>>(p);
+    } else {
+        if (p.ref) fwd3d_generic<DT, G, 0, 0, true><<<grid, block, 0, s>>>(p);
+        else fwd3d_generic<DT, G, 0, 0, false><<<grid, block, 0, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+// All lane-group widths G (lanes per value row at 16 bytes per lane) for one dtype and
+// dimensionality.
+template <int DT, int NDIM>
+cudaError_t forward_dispatch(int G, const Params &p, cudaStream_t s) {
+    switch (G) {
+        case 1: return forward_nd<DT, 1, NDIM>(p, s);
+        case 2: return forward_nd<DT, 2, NDIM>(p, s);
+        case 4: return forward_nd<DT, 4, NDIM>(p, s);
+        case 8: return forward_nd<DT, 8, NDIM>(p, s);
+        case 16: return forward_nd<DT, 16, NDIM>(p, s);
+        case 32: return forward_nd<DT, 32, NDIM>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+}  // namespace msda

@@ -1,0 +1,10 @@
+// Forward kernels instantiated for bf16 values, 2D (see msda_forward.cuh).
+#include "msda_forward.cuh"
+
+namespace msda {
+
+cudaError_t launch_forward_bf16_2d(int G, const Params &p, cudaStream_t s) {
+    return forward_dispatch<kBF16, 2>(G, p, s);
+}
+
+}  // namespace msda

@@ -51,6 +51,14 @@ cudaError_t launch_forward(int ndim, int dtype, int G, const Params &p, cudaStre
 cudaError_t launch_backward(int ndim, int dtype, int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_zero_fill(float *ptr, long long n_floats, cudaStream_t stream);
 
+// Per-(dtype, ndim) instantiations behind launch_forward / launch_backward.
+cudaError_t launch_forward_f32_2d(int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_forward_f32_3d(int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_forward_bf16_2d(int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_forward_bf16_3d(int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_backward_2d(int dtype, int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_backward_3d(int dtype, int G, const Params &p, cudaStream_t stream);
+
 // Query order (msda_order.cu): sorts each batch's queries by the Morton code of the mean
 // of their sampling locations.  `hist` holds B * kOrderBuckets ints, `keys` B * Nq ints.
 constexpr int kOrderBits2d = 6;    // bits per axis of the 2D key (64 x 64 cells)
