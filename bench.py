@@ -83,10 +83,12 @@ def kernel_source_hash(kind: str = "forward") -> str:
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, mode: str = ""):
     """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if it was
-    taken on the current sources of that kernel family (else None)."""
+    taken on the current sources of that kernel family (else None).  A summary names its
+    bench workload, with "+order" / "+fused" / "+prune<t>" appended for those modes."""
     src = kernel_source_hash("backward" if workloads.WORKLOADS[workload].backward else "forward")
+    key = workload + mode
     if not os.path.isdir(PROFILE_DIR):
         return None
     for f in sorted(os.listdir(PROFILE_DIR)):
@@ -96,7 +98,7 @@ def recorded_traffic(workload: str):
         m_w = re.search(r"^bench_workload:\s*(\S+)", text, re.M)
         m_h = re.search(r"^kernel_source_sha256:\s*([0-9a-f]{64})", text, re.M)
         m_t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-        if m_w and m_h and m_t and m_w.group(1) == workload and m_h.group(1) == src:
+        if m_w and m_h and m_t and m_w.group(1) == key and m_h.group(1) == src:
             return float(m_t.group(1))
     return None
 
@@ -542,7 +544,8 @@ def run_ours(args):
     peak, peak_src = measured_peaks()
     per_launch_s = t_rank / args.steps
     achieved = ab["total"] / per_launch_s / 1e9
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w.name, "+order" if args.order else "+fused" if args.fused else
+                               f"+prune{args.prune:g}" if args.prune > 0 else "")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
