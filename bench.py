@@ -551,9 +551,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "Nin": w.Nin, "Nq": w.Nq, "M": w.M,
-                   "D": w.D, "L": w.L, "P": w.P, "levels": [list(s) for s in w.shapes],
-                   "ndim": w.ndim, "pass": "backward" if w.backward else "forward",
+        "config": {**workload_config(w),
                    "query_order": "computed each step (msda_query_order) and used by the "
                                   "ordered forward" if args.order else "as given",
                    "prologue": ("fused: reference points + pixel offsets + logits in, "
@@ -562,7 +560,6 @@ def run_ours(args):
                    "prune": (f"samples with |A| < {args.prune} skipped "
                              f"({float((np.abs(inp['attention_weights']) < args.prune).mean()):.3f}"
                              " of them): an approximation") if args.prune > 0 else "none (exact)",
-                   "samples_per_step_per_gpu": w.samples,
                    "l2": f"cold: {n_sets} rotating input sets of {set_bytes / 1e6:.1f} MB "
                          f"(> 2x L2) between steps",
                    "parallelism": f"weak: {world} rank(s), one batch each, no collective"},
@@ -689,6 +686,14 @@ def run_e2e(msda, w, inp, dev, args, world):
 # ----------------------------------------------------------------------------- reference arm
 
 
+def workload_config(w: workloads.Workload) -> dict:
+    """The workload keys of the JSON line's `config`, the same on both arms."""
+    return {"workload": w.name, "B": w.B, "Nin": w.Nin, "Nq": w.Nq, "M": w.M, "D": w.D,
+            "L": w.L, "P": w.P, "levels": [list(s) for s in w.shapes], "ndim": w.ndim,
+            "value_dtype": w.dtype, "pass": "backward" if w.backward else "forward",
+            "samples_per_step_per_gpu": w.samples}
+
+
 def run_reference(args):
     """The CPU oracle as it stands, timed on the host cores on this arm's workload and
     metric; each step is a bounded sample (a contiguous block of queries of batch 0)."""
@@ -736,9 +741,7 @@ def run_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "Nin": w.Nin, "Nq": w.Nq, "M": w.M,
-                       "D": w.D, "L": w.L, "P": w.P,
-                       "pass": "backward" if w.backward else "forward"},
+            "config": workload_config(w),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
