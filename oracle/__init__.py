@@ -188,6 +188,33 @@ def forward_fused(nd: int, value, spatial_shapes, level_start_index, reference_p
                    softmax_weights(attention_logits), lib=lib)
 
 
+def backward_fused(nd: int, value, spatial_shapes, level_start_index, reference_points,
+                   sampling_offsets, attention_logits, grad_out, lib=None):
+    """Gradients of ``forward_fused`` ("3D Attention That Knows Where to Look": gradients
+    flow back into both the offsets and the weights; "Deformable Attention Module": the
+    weights are a softmax of the predicted logits), by the chain rule through the prologue,
+    in double:
+
+      grad_offset[b,q,m,l,p,k] = grad_location[b,q,m,l,p,k] / E_lk  (location = ref + offset / E)
+      grad_logit[b,q,m,s]      = A_s * (grad_A_s - sum_t A_t * grad_A_t)  over the item's L x P
+      grad_ref[b,q,l,k]        = sum over m and p of grad_location[b,q,m,l,p,k]
+
+    where grad_value, grad_location and grad_A are the core's backward at the fused
+    locations and weights.  Returns (grad_value, grad_offsets, grad_logits, grad_ref)."""
+    sh = np.asarray(spatial_shapes, dtype=np.int64)
+    loc = fused_locations(sh, reference_points, sampling_offsets)
+    a = softmax_weights(attention_logits)
+    gv, gl, ga = backward(nd, value, sh, level_start_index, loc, a, grad_out, lib=lib)
+    ext = sh[:, ::-1].astype(np.float64)                              # [L, nd] = (W, H[, Z])
+    g_off = gl / ext[None, None, None, :, None, :]
+    B, Nq, M, L, P = a.shape
+    a2 = a.reshape(B, Nq, M, L * P)
+    g2 = ga.reshape(B, Nq, M, L * P)
+    g_logit = (a2 * (g2 - (a2 * g2).sum(axis=-1, keepdims=True))).reshape(a.shape)
+    g_ref = gl.sum(axis=(2, 4))                                       # [B, Nq, L, nd]
+    return gv, g_off, g_logit, g_ref
+
+
 def forward_pruned(nd: int, value, spatial_shapes, level_start_index, sampling_locations,
                    attention_weights, threshold: float, lib=None) -> np.ndarray:
     """The core with probability-aware pruning of sampling points ("DEFA: Efficient

@@ -175,3 +175,91 @@ def test_fused_oracle_invariants(oracle_mod):
     # the weights of every (query, head) sum to one
     a = oracle_mod.softmax_weights(f["attention_logits"])
     assert np.allclose(a.reshape(a.shape[:3] + (-1,)).sum(-1), 1.0, atol=1e-12)
+
+
+def _fused_case(nd, seed):
+    rng = np.random.default_rng(seed)
+    shapes = np.array([(5, 7), (3, 4)] if nd == 2 else [(3, 4, 5), (2, 3, 3)], dtype=np.int64)
+    L = len(shapes)
+    B, Nq, M, P, D = 2, 3, 2, 3, 3
+    Nin = int(np.prod(shapes, axis=1).sum())
+    starts = np.concatenate([[0], np.cumsum(np.prod(shapes, axis=1))[:-1]])
+    return dict(value=rng.standard_normal((B, Nin, M, D)), spatial_shapes=shapes,
+                level_start_index=starts,
+                reference_points=rng.uniform(0.2, 0.8, (B, Nq, L, nd)).astype(np.float32),
+                sampling_offsets=(rng.standard_normal((B, Nq, M, L, P, nd)) * 1.5).astype(
+                    np.float32),
+                attention_logits=rng.standard_normal((B, Nq, M, L, P)).astype(np.float32),
+                grad_out=rng.standard_normal((B, Nq, M * D)), rng=rng)
+
+
+@pytest.mark.parametrize("nd", [2, 3])
+def test_fused_backward_matches_finite_differences_of_the_fused_forward(oracle_mod, nd):
+    """The fused prologue's gradients against central differences of forward_fused: in the
+    logits (double softmax, small step), in the pixel offsets and in the reference points
+    (fp32 locations, a 0.02-pixel step kept inside every sample's cell: the interpolation
+    is quadratic along a line there, so the central difference is exact up to rounding),
+    and the value adjoint."""
+    c = _fused_case(nd, 70 + nd)
+    rng = c.pop("rng")
+    g = c["grad_out"]
+    base = (nd, c["value"], c["spatial_shapes"], c["level_start_index"])
+    gv, g_off, g_logit, g_ref = oracle_mod.backward_fused(
+        *base, c["reference_points"], c["sampling_offsets"], c["attention_logits"], g)
+
+    def f(ref=None, off=None, z=None):
+        out = oracle_mod.forward_fused(
+            *base, c["reference_points"] if ref is None else ref,
+            c["sampling_offsets"] if off is None else off,
+            c["attention_logits"] if z is None else z)
+        return float(np.sum(g * out))
+
+    # logits
+    dz = rng.standard_normal(c["attention_logits"].shape)
+    z0 = c["attention_logits"].astype(np.float64)
+    h = 1e-5
+    fd = (f(z=z0 + h * dz) - f(z=z0 - h * dz)) / (2 * h)
+    an = float(np.sum(g_logit * dz))
+    assert abs(fd - an) <= 1e-7 * (1 + abs(an)), (fd, an)
+    # offsets and reference points: only coordinates at least 0.1 px from a kink move
+    ext = c["spatial_shapes"][:, ::-1].astype(np.float64)[None, None, None, :, None, :]
+    loc = oracle_mod.fused_locations(c["spatial_shapes"], c["reference_points"],
+                                     c["sampling_offsets"]).astype(np.float64)
+    pix = loc * ext - 0.5
+    smooth = np.abs(pix - np.round(pix)) > 0.1
+    step = 0.02                                                      # pixels
+    d_off = np.where(smooth, rng.standard_normal(pix.shape), 0.0)
+    o0 = c["sampling_offsets"].astype(np.float64)
+    fd = (f(off=(o0 + step * d_off).astype(np.float32)) -
+          f(off=(o0 - step * d_off).astype(np.float32))) / (2 * step)
+    an = float(np.sum(g_off * d_off))
+    mag = float(np.sum(np.abs(g_off * d_off)))
+    assert abs(fd - an) <= 2e-3 * (1e-3 + mag), (fd, an)
+    # a reference coordinate moves every sample of its (b, q, l) along that axis
+    ref_smooth = smooth.all(axis=(2, 4))                             # [B, Nq, L, nd]
+    d_ref = np.where(ref_smooth, rng.standard_normal(ref_smooth.shape), 0.0)
+    assert d_ref.any()
+    hr = step / ext[0, 0, 0, :, 0, :][None, None]                    # 0.02 px in each axis
+    r0 = c["reference_points"].astype(np.float64)
+    fd = (f(ref=(r0 + hr * d_ref).astype(np.float32)) -
+          f(ref=(r0 - hr * d_ref).astype(np.float32))) / (2 * step)
+    an = float(np.sum(g_ref * d_ref * hr / step))
+    mag = float(np.sum(np.abs(g_ref * d_ref * hr / step)))
+    assert abs(fd - an) <= 2e-3 * (1e-3 + mag), (fd, an)
+    # value: linear, so the adjoint identity holds exactly up to rounding
+    out = oracle_mod.forward_fused(*base, c["reference_points"], c["sampling_offsets"],
+                                   c["attention_logits"])
+    assert abs(float(np.sum(c["value"] * gv)) - float(np.sum(g * out))) <= 1e-10 * (
+        1 + float(np.sum(np.abs(g * out))))
+
+
+def test_fused_backward_logit_gradients_sum_to_zero(oracle_mod):
+    """The softmax is unchanged by adding a constant to an item's logits, so the logit
+    gradients of every (query, head) sum to zero."""
+    c = _fused_case(2, 80)
+    c.pop("rng")
+    _, _, g_logit, _ = oracle_mod.backward_fused(
+        2, c["value"], c["spatial_shapes"], c["level_start_index"], c["reference_points"],
+        c["sampling_offsets"], c["attention_logits"], c["grad_out"])
+    s = g_logit.reshape(g_logit.shape[:3] + (-1,)).sum(-1)
+    assert np.allclose(s, 0.0, atol=1e-12)
