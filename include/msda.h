@@ -161,6 +161,44 @@ msda_status msda3d_forward_fused(const msda_dims *dims, const void *value,
                                  const float *attention_logits, void *out, msda_stream_t stream);
 
 /*
+ * Backward of msda2d_forward_fused / msda3d_forward_fused: the gradients of
+ * sum(grad_out * out) with respect to value, the sampling offsets, the attention logits
+ * and (optionally) the reference points ("3D Attention That Knows Where to Look": gradients
+ * flow back into both the offsets and the weights; "Deformable Attention Module": the
+ * weights are a softmax of predicted logits).  With grad_location and grad_A the core's
+ * gradients at the fused locations and weights (as msda2d_backward defines them):
+ *   grad_sampling_offsets[b,q,m,l,p,k] = grad_location[b,q,m,l,p,k] / E_lk
+ *   grad_attention_logits[b,q,m,s]     = A_s * (grad_A_s - sum_t A_t * grad_A_t)
+ *                                        (s, t over the item's L x P samples)
+ *   grad_reference_points[b,q,l,k]     = sum over m and p of grad_location[b,q,m,l,p,k]
+ *   grad_sampling_offsets  [B, Nq, M, L, P, 2|3] fp32, overwritten
+ *   grad_attention_logits  [B, Nq, M, L, P]      fp32, overwritten
+ *   grad_reference_points  [B, Nq, L, 2|3]       fp32, overwritten; may be NULL when the
+ *                                                reference points need no gradient
+ * grad_value is zero-filled by the call and accumulated with fp32 atomics, as in
+ * msda2d_backward.  The locations and weights are formed exactly as the fused forward
+ * forms them; the logit gradients are finished by a second small kernel on the same
+ * stream and the reference-point gradients (a sum in the order m, p) by a third.  All
+ * other arguments, limits and errors are those of msda2d_backward / msda3d_backward and
+ * msda2d_forward_fused.
+ */
+msda_status msda2d_backward_fused(const msda_dims *dims, const void *value,
+                                  const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                  const float *reference_points, const float *sampling_offsets,
+                                  const float *attention_logits, const void *grad_out,
+                                  float *grad_value, float *grad_sampling_offsets,
+                                  float *grad_attention_logits, float *grad_reference_points,
+                                  msda_stream_t stream);
+
+msda_status msda3d_backward_fused(const msda_dims *dims, const void *value,
+                                  const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                  const float *reference_points, const float *sampling_offsets,
+                                  const float *attention_logits, const void *grad_out,
+                                  float *grad_value, float *grad_sampling_offsets,
+                                  float *grad_attention_logits, float *grad_reference_points,
+                                  msda_stream_t stream);
+
+/*
  * Probability-aware pruning of sampling points (an opt-in approximation; "DEFA: Efficient
  * Deformable Attention Acceleration via Pruning-Assisted Grid-Sampling and Multi-Scale
  * Parallel Processing", abstract: pruning of sampling points by their probability).

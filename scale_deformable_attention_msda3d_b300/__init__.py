@@ -6,9 +6,10 @@ The compute path is libmsda.so (hand-written sm_103a CUDA kernels behind the C A
     msda2d_forward, msda2d_backward, msda3d_forward, msda3d_backward,
     msda_query_order, msda2d_forward_ordered, msda3d_forward_ordered,
     msda2d_forward_pruned, msda3d_forward_pruned, msda2d_forward_fused, msda3d_forward_fused,
-    msda_last_error, msda_abi_version
+    msda2d_backward_fused, msda3d_backward_fused, msda_last_error, msda_abi_version
 
-plus ``MSDeformAttnFunction`` (torch.autograd) for use inside a model.  The library is
+plus ``MSDeformAttnFunction`` / ``ms_deform_attn`` and ``ms_deform_attn_fused``
+(torch.autograd) for use inside a model.  The library is
 built in-tree by ``python -m scale_deformable_attention_msda3d_b300.build`` (or on first
 use when missing); without it every call raises -- there is no CPU fallback.
 """
@@ -17,9 +18,10 @@ from ._binding import (EXPORTS, MSDA_BF16, MSDA_ERR_CUDA, MSDA_ERR_INTERNAL,  # 
                        MSDA_MAX_POINTS, MSDA_OK, MsdaError, backward_raw, forward_ordered_raw,
                        forward_pruned_raw, msda2d_forward_pruned, msda3d_forward_pruned,
                        forward_fused_raw, msda2d_forward_fused, msda3d_forward_fused,
+                       backward_fused_raw, msda2d_backward_fused, msda3d_backward_fused,
                        forward_raw, library_path, load, make_dims, msda2d_backward,
                        msda2d_forward, msda2d_forward_ordered, msda3d_backward,
                        msda3d_forward, msda3d_forward_ordered, msda_abi_version, msda_dims,
                        msda_last_error, msda_query_order, query_order_raw, query_order_static_raw,
                        query_order_workspace_bytes, query_order_workspace_raw)
-from .autograd import MSDeformAttnFunction, ms_deform_attn  # noqa: F401
+from .autograd import MSDeformAttnFunction, ms_deform_attn, ms_deform_attn_fused  # noqa: F401

@@ -27,7 +27,8 @@ EXPORTS = ("msda2d_forward", "msda2d_backward", "msda3d_forward", "msda3d_backwa
            "msda_last_error", "msda_abi_version", "msda_query_order",
            "msda_query_order_workspace_size", "msda2d_forward_ordered", "msda3d_forward_ordered",
            "msda_query_order_static", "msda2d_forward_pruned", "msda3d_forward_pruned",
-           "msda2d_forward_fused", "msda3d_forward_fused")
+           "msda2d_forward_fused", "msda3d_forward_fused", "msda2d_backward_fused",
+           "msda3d_backward_fused")
 
 
 class MsdaError(RuntimeError):
@@ -89,6 +90,10 @@ def load(path: Optional[str] = None):
         lib.msda_query_order.restype = ctypes.c_int
         for name in ("msda2d_forward_fused", "msda3d_forward_fused"):
             getattr(lib, name).argtypes = [_DIMS_P, _VP, _I64P, _I64P, _VP, _VP, _VP, _VP, _VP]
+            getattr(lib, name).restype = ctypes.c_int
+        for name in ("msda2d_backward_fused", "msda3d_backward_fused"):
+            getattr(lib, name).argtypes = [_DIMS_P, _VP, _I64P, _I64P, _VP, _VP, _VP, _VP, _VP,
+                                           _VP, _VP, _VP, _VP]
             getattr(lib, name).restype = ctypes.c_int
         fwd_p = [_DIMS_P, _VP, _I64P, _I64P, _VP, _VP, ctypes.c_float, _VP, _VP]
         for name in ("msda2d_forward_pruned", "msda3d_forward_pruned"):
@@ -212,6 +217,23 @@ def backward_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes, level_s
               ls.ctypes.data_as(_I64P), _VP(sampling_locations), _VP(attention_weights),
               _VP(grad_out), _VP(grad_value), _VP(grad_sampling_locations),
               _VP(grad_attention_weights), _VP(stream))
+
+
+def backward_fused_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes,
+                       level_start_index, reference_points: int, sampling_offsets: int,
+                       attention_logits: int, grad_out: int, grad_value: int,
+                       grad_sampling_offsets: int, grad_attention_logits: int,
+                       grad_reference_points: int = 0, stream: int = 0, lib=None) -> int:
+    """Call msda{2,3}d_backward_fused with raw device pointers (grad_reference_points 0 =
+    not wanted); returns the status (no raise)."""
+    lib = lib or load()
+    sh, ls = _host_i64(spatial_shapes), _host_i64(level_start_index)
+    fn = lib.msda2d_backward_fused if ndim == 2 else lib.msda3d_backward_fused
+    return fn(ctypes.byref(dims), _VP(value), sh.ctypes.data_as(_I64P),
+              ls.ctypes.data_as(_I64P), _VP(reference_points), _VP(sampling_offsets),
+              _VP(attention_logits), _VP(grad_out), _VP(grad_value),
+              _VP(grad_sampling_offsets), _VP(grad_attention_logits),
+              _VP(grad_reference_points or None), _VP(stream))
 
 
 # ----------------------------------------------------------------------------- torch layer
@@ -465,6 +487,58 @@ def msda3d_forward_fused(value, spatial_shapes, level_start_index, reference_poi
     """3D forward with the prologue fused (offsets in voxels of the sampled level)."""
     return _forward_fused(3, value, spatial_shapes, level_start_index, reference_points,
                           sampling_offsets, attention_logits, out, stream)
+
+
+def _backward_fused(ndim, value, spatial_shapes, level_start_index, reference_points,
+                    sampling_offsets, attention_logits, grad_out, need_reference_grad=True,
+                    stream=None):
+    torch = _torch()
+    dims = _dims_from(value, sampling_offsets, ndim)
+    _require(value, "value")
+    _require(reference_points, "reference_points", torch.float32)
+    _require(sampling_offsets, "sampling_offsets", torch.float32)
+    _require(attention_logits, "attention_logits", torch.float32)
+    _require(grad_out, "grad_out", value.dtype)
+    if tuple(reference_points.shape) != (dims.B, dims.Nq, dims.L, ndim):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, f"reference_points must be [B, Nq, L, {ndim}]")
+    if tuple(attention_logits.shape) != tuple(sampling_offsets.shape[:-1]):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "attention_logits must be [B, Nq, M, L, P]")
+    if tuple(grad_out.shape) != (dims.B, dims.Nq, dims.M * dims.D):
+        raise MsdaError(MSDA_ERR_INVALID_ARG, "grad_out must be [B, Nq, M*D]")
+    dev = value.device
+    grad_value = torch.empty(value.shape, dtype=torch.float32, device=dev)
+    grad_off = torch.empty_like(sampling_offsets)
+    grad_logits = torch.empty_like(attention_logits)
+    grad_ref = torch.empty_like(reference_points) if need_reference_grad else None
+    lib = load()
+    st = backward_fused_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
+                            reference_points.data_ptr(), sampling_offsets.data_ptr(),
+                            attention_logits.data_ptr(), grad_out.data_ptr(),
+                            grad_value.data_ptr(), grad_off.data_ptr(), grad_logits.data_ptr(),
+                            grad_ref.data_ptr() if grad_ref is not None else 0,
+                            _stream_handle(stream, dev), lib=lib)
+    _check(lib, st)
+    return grad_value, grad_off, grad_logits, grad_ref
+
+
+def msda2d_backward_fused(value, spatial_shapes, level_start_index, reference_points,
+                          sampling_offsets, attention_logits, grad_out, need_reference_grad=True,
+                          stream=None):
+    """Backward of msda2d_forward_fused.  Returns (grad_value fp32, grad_sampling_offsets,
+    grad_attention_logits, grad_reference_points or None when need_reference_grad is
+    False)."""
+    return _backward_fused(2, value, spatial_shapes, level_start_index, reference_points,
+                           sampling_offsets, attention_logits, grad_out, need_reference_grad,
+                           stream)
+
+
+def msda3d_backward_fused(value, spatial_shapes, level_start_index, reference_points,
+                          sampling_offsets, attention_logits, grad_out, need_reference_grad=True,
+                          stream=None):
+    """Backward of msda3d_forward_fused (see msda2d_backward_fused)."""
+    return _backward_fused(3, value, spatial_shapes, level_start_index, reference_points,
+                           sampling_offsets, attention_logits, grad_out, need_reference_grad,
+                           stream)
 
 
 def msda2d_forward_pruned(value, spatial_shapes, level_start_index, sampling_locations,

@@ -60,3 +60,53 @@ def ms_deform_attn(value, spatial_shapes, level_start_index, sampling_locations,
     ``sampling_locations``).  ``spatial_shapes`` / ``level_start_index`` are host arrays."""
     return MSDeformAttnFunction.apply(value, spatial_shapes, level_start_index,
                                       sampling_locations, attention_weights)
+
+
+class _FusedFn:
+    """Lazily built autograd.Function for the fused-prologue call."""
+    cls = None
+
+    @classmethod
+    def get(cls):
+        if cls.cls is None:
+            torch = _import_torch()
+
+            class MSDeformAttnFused(torch.autograd.Function):
+                @staticmethod
+                def forward(ctx, value, spatial_shapes, level_start_index, reference_points,
+                            sampling_offsets, attention_logits):
+                    ndim = sampling_offsets.shape[-1]
+                    shapes = np.asarray(spatial_shapes, dtype=np.int64)
+                    starts = np.asarray(level_start_index, dtype=np.int64)
+                    fwd = (_binding.msda2d_forward_fused if ndim == 2
+                           else _binding.msda3d_forward_fused)
+                    out = fwd(value, shapes, starts, reference_points, sampling_offsets,
+                              attention_logits)
+                    ctx.save_for_backward(value, reference_points, sampling_offsets,
+                                          attention_logits)
+                    ctx.meta = (ndim, shapes, starts)
+                    return out
+
+                @staticmethod
+                def backward(ctx, grad_out):
+                    value, ref, off, logits = ctx.saved_tensors
+                    ndim, shapes, starts = ctx.meta
+                    bwd = (_binding.msda2d_backward_fused if ndim == 2
+                           else _binding.msda3d_backward_fused)
+                    gv, goff, gz, gref = bwd(value, shapes, starts, ref, off, logits,
+                                             grad_out.contiguous(),
+                                             need_reference_grad=ctx.needs_input_grad[3])
+                    return gv.to(value.dtype), None, None, gref, goff, gz
+
+            cls.cls = MSDeformAttnFused
+        return cls.cls
+
+
+def ms_deform_attn_fused(value, spatial_shapes, level_start_index, reference_points,
+                         sampling_offsets, attention_logits):
+    """Differentiable core with the module's prologue fused in: location = reference point
+    + offset / extent (offsets in pixels of the sampled level), weights = softmax of the
+    logits over each query and head's L x P samples.  Gradients flow to value, the
+    reference points, the offsets and the logits."""
+    return _FusedFn.get().apply(value, spatial_shapes, level_start_index, reference_points,
+                                sampling_offsets, attention_logits)

@@ -116,6 +116,14 @@ __device__ __forceinline__ float group_sum(float v) {
     return v;
 }
 
+// Maximum over the G lanes of a lane group (same contract as group_sum).
+template <int G>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
 // Work item (b, q, m) at launch position `pos`.  Positions run over (b, i, m); the query
 // is q = order[b * Nq + i] when a query order is given, else i.  Order entries are clamped
 // into [0, Nq), so a malformed order gives wrong results but no out-of-range access.
@@ -137,6 +145,15 @@ __device__ __forceinline__ float fused_location(const Params &p, long long bq, i
     const float ext = k == 0 ? p.fW[l] : (k == 1 ? p.fH[l] : p.fZ[l]);
     const float r = __ldg(p.ref + (bq * p.L + l) * NDIM + k);
     return __fadd_rn(r, __fdiv_rn(offset, ext));
+}
+
+// Softmax statistics of an item's S logits (fused prologue, generic kernels and the
+// backward epilogue): max and the sum of expf(z - max).
+__device__ __forceinline__ void logit_stats(const float *z, int S, float &mx, float &sum) {
+    mx = -INFINITY;
+    for (int i = 0; i < S; ++i) mx = fmaxf(mx, __ldg(z + i));
+    sum = 0.f;
+    for (int i = 0; i < S; ++i) sum += expf(__ldg(z + i) - mx);
 }
 
 // ------------------------------------------------------------------ per-sample taps

@@ -148,8 +148,8 @@ msda_status forward_impl(int ndim, const msda_dims *dims, const void *value,
     MSDA_TRY(build_params(dims, ndim, shapes, level_start, &p, &G));
     if (p.n_items == 0) return MSDA_OK;  // empty batch or no queries: nothing to compute
     MSDA_TRY(check_ptr(value, "value"));
-    MSDA_TRY(check_ptr(loc, "sampling_locations"));
-    MSDA_TRY(check_ptr(attn, "attention_weights"));
+    MSDA_TRY(check_ptr(loc, fused ? "sampling_offsets" : "sampling_locations"));
+    MSDA_TRY(check_ptr(attn, fused ? "attention_logits" : "attention_weights"));
     MSDA_TRY(check_ptr(out, "out"));
     if (ordered) {
         if (!order) return fail(MSDA_ERR_INVALID_ARG, "query_order is NULL");
@@ -175,7 +175,9 @@ msda_status forward_impl(int ndim, const msda_dims *dims, const void *value,
 msda_status backward_impl(int ndim, const msda_dims *dims, const void *value,
                           const int64_t *shapes, const int64_t *level_start, const float *loc,
                           const float *attn, const void *grad_out, float *grad_value,
-                          float *grad_loc, float *grad_attn, msda_stream_t stream) {
+                          float *grad_loc, float *grad_attn, msda_stream_t stream,
+                          const float *ref = nullptr, float *grad_ref = nullptr,
+                          bool fused = false) {
     msda::Params p;
     int G = 0;
     MSDA_TRY(build_params(dims, ndim, shapes, level_start, &p, &G));
@@ -184,11 +186,15 @@ msda_status backward_impl(int ndim, const msda_dims *dims, const void *value,
     MSDA_TRY(check_ptr(grad_value, "grad_value"));
     if (p.n_items > 0) {
         MSDA_TRY(check_ptr(value, "value"));
-        MSDA_TRY(check_ptr(loc, "sampling_locations"));
-        MSDA_TRY(check_ptr(attn, "attention_weights"));
+        MSDA_TRY(check_ptr(loc, fused ? "sampling_offsets" : "sampling_locations"));
+        MSDA_TRY(check_ptr(attn, fused ? "attention_logits" : "attention_weights"));
         MSDA_TRY(check_ptr(grad_out, "grad_out"));
-        MSDA_TRY(check_ptr(grad_loc, "grad_sampling_locations"));
-        MSDA_TRY(check_ptr(grad_attn, "grad_attention_weights"));
+        MSDA_TRY(check_ptr(grad_loc, fused ? "grad_sampling_offsets" : "grad_sampling_locations"));
+        MSDA_TRY(check_ptr(grad_attn, fused ? "grad_attention_logits" : "grad_attention_weights"));
+        if (fused) {
+            MSDA_TRY(check_ptr(ref, "reference_points"));
+            if (grad_ref) MSDA_TRY(check_ptr(grad_ref, "grad_reference_points"));
+        }
     }
     MSDA_TRY(cuda_status(msda::launch_zero_fill(grad_value, p.B * p.Nin * p.M * p.D, s),
                          "grad_value zero-fill launch"));
@@ -199,8 +205,10 @@ msda_status backward_impl(int ndim, const msda_dims *dims, const void *value,
     p.grad_value = grad_value;
     p.grad_loc = grad_loc;
     p.grad_attn = grad_attn;
+    p.ref = fused ? ref : nullptr;
+    p.grad_ref = fused ? grad_ref : nullptr;
     return cuda_status(msda::launch_backward(ndim, dims->value_dtype, G, p, s),
-                       "backward launch");
+                       fused ? "fused backward launch" : "backward launch");
 }
 
 // Workspace of msda_query_order: per-batch histogram, then per-query keys (256-byte aligned).
@@ -387,8 +395,34 @@ msda_status msda3d_backward(const msda_dims *dims, const void *value,
                          grad_attention_weights, stream);
 }
 
+msda_status msda2d_backward_fused(const msda_dims *dims, const void *value,
+                                  const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                  const float *reference_points, const float *sampling_offsets,
+                                  const float *attention_logits, const void *grad_out,
+                                  float *grad_value, float *grad_sampling_offsets,
+                                  float *grad_attention_logits, float *grad_reference_points,
+                                  msda_stream_t stream) {
+    return backward_impl(2, dims, value, spatial_shapes, level_start_index, sampling_offsets,
+                         attention_logits, grad_out, grad_value, grad_sampling_offsets,
+                         grad_attention_logits, stream, reference_points, grad_reference_points,
+                         true);
+}
+
+msda_status msda3d_backward_fused(const msda_dims *dims, const void *value,
+                                  const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                  const float *reference_points, const float *sampling_offsets,
+                                  const float *attention_logits, const void *grad_out,
+                                  float *grad_value, float *grad_sampling_offsets,
+                                  float *grad_attention_logits, float *grad_reference_points,
+                                  msda_stream_t stream) {
+    return backward_impl(3, dims, value, spatial_shapes, level_start_index, sampling_offsets,
+                         attention_logits, grad_out, grad_value, grad_sampling_offsets,
+                         grad_attention_logits, stream, reference_points, grad_reference_points,
+                         true);
+}
+
 const char *msda_last_error(void) { return g_err; }
 
-int32_t msda_abi_version(void) { return 10100; }
+int32_t msda_abi_version(void) { return 10200; }
 
 }  // extern "C"

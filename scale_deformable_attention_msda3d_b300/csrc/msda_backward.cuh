@@ -47,7 +47,7 @@ __device__ __forceinline__ float dot(const uint4 &u, const float (&g)[N]) {
     return s;
 }
 
-template <int DT, int G, int LL, int PP>
+template <int DT, int G, int LL, int PP, bool FUSED>
 __global__ void __launch_bounds__(256)
 bwd2d_generic(const __grid_constant__ Params p) {
     constexpr int N = Vec<DT>::N;
@@ -71,18 +71,28 @@ bwd2d_generic(const __grid_constant__ Params p) {
     unpack(ldg16(static_cast<const char *>(p.grad_out) + item * (rb / p.M) + sub * 16), g);
     const long long s0 = item * L * P;
     const float2 *lp = reinterpret_cast<const float2 *>(p.loc) + s0;
+    float zmax = 0.f, zsum = 1.f;
+    if constexpr (FUSED) logit_stats(p.attn + s0, L * P, zmax, zsum);
 
 #pragma unroll
     for (int l = 0; l < L; ++l) {
         const int W = p.W[l], H = p.H[l];
         const float fW = p.fW[l], fH = p.fH[l];
+        // fused: the gradient goes to the offset, d location / d offset = 1 / extent
+        const float eW = FUSED ? 1.f : fW, eH = FUSED ? 1.f : fH;
         const char *vl = vb + static_cast<long long>(p.start[l]) * rb;
         float *gl = gvb + static_cast<long long>(p.start[l]) * rowf;
 #pragma unroll 2
         for (int k = 0; k < P; ++k) {
             const long long s = s0 + l * P + k;
-            const float2 xy = __ldg(lp + l * P + k);
-            const float a = __ldg(p.attn + s);
+            float2 xy = __ldg(lp + l * P + k);
+            float a = __ldg(p.attn + s);
+            if constexpr (FUSED) {
+                const long long bq = item / p.M;
+                xy.x = fused_location<2>(p, bq, l, 0, xy.x);
+                xy.y = fused_location<2>(p, bq, l, 1, xy.y);
+                a = __fdiv_rn(expf(a - zmax), zsum);
+            }
             int x0, y0;
             float fx, fy;
             const bool okx = pixel_coord(xy.x, fW, x0, fx);
@@ -110,9 +120,9 @@ bwd2d_generic(const __grid_constant__ Params p) {
             if (active) {
                 if (sub == 0) {
                     const bool any = ok00 || ok01 || ok10 || ok11;
-                    p.grad_attn[s] = gA;
-                    p.grad_loc[2 * s] = any ? a * gx * fW : 0.f;
-                    p.grad_loc[2 * s + 1] = any ? a * gy * fH : 0.f;
+                    p.grad_attn[s] = gA;  // fused: grad_A, turned into d/d logits later
+                    p.grad_loc[2 * s] = any ? a * gx * eW : 0.f;
+                    p.grad_loc[2 * s + 1] = any ? a * gy * eH : 0.f;
                 }
                 float *d = gl + r00 * rowf;
                 if (ok00) scatter<N>(d, a * (wy0 * wx0), g);
@@ -124,7 +134,7 @@ bwd2d_generic(const __grid_constant__ Params p) {
     }
 }
 
-template <int DT, int G, int LL, int PP>
+template <int DT, int G, int LL, int PP, bool FUSED>
 __global__ void __launch_bounds__(256)
 bwd3d_generic(const __grid_constant__ Params p) {
     constexpr int N = Vec<DT>::N;
@@ -146,24 +156,34 @@ bwd3d_generic(const __grid_constant__ Params p) {
     float g[N];
     unpack(ldg16(static_cast<const char *>(p.grad_out) + item * (rb / p.M) + sub * 16), g);
     const long long s0 = item * L * P;
+    float zmax = 0.f, zsum = 1.f;
+    if constexpr (FUSED) logit_stats(p.attn + s0, L * P, zmax, zsum);
 
 #pragma unroll
     for (int l = 0; l < L; ++l) {
         const int W = p.W[l], H = p.H[l], Z = p.Z[l];
         const float fW = p.fW[l], fH = p.fH[l], fZ = p.fZ[l];
+        const float eW = FUSED ? 1.f : fW, eH = FUSED ? 1.f : fH, eZ = FUSED ? 1.f : fZ;
         const char *vl = vb + static_cast<long long>(p.start[l]) * rb;
         float *gl = gvb + static_cast<long long>(p.start[l]) * rowf;
         const long long HW = static_cast<long long>(H) * W;
 #pragma unroll 1
         for (int k = 0; k < P; ++k) {
             const long long s = s0 + l * P + k;
-            const float *xyz = p.loc + 3 * s;
-            const float a = __ldg(p.attn + s);
+            float xyz[3] = {__ldg(p.loc + 3 * s), __ldg(p.loc + 3 * s + 1),
+                            __ldg(p.loc + 3 * s + 2)};
+            float a = __ldg(p.attn + s);
+            if constexpr (FUSED) {
+                const long long bq = item / p.M;
+#pragma unroll
+                for (int c = 0; c < 3; ++c) xyz[c] = fused_location<3>(p, bq, l, c, xyz[c]);
+                a = __fdiv_rn(expf(a - zmax), zsum);
+            }
             int x0, y0, z0;
             float fx, fy, fz;
-            const bool valid = pixel_coord(__ldg(xyz), fW, x0, fx) &
-                               pixel_coord(__ldg(xyz + 1), fH, y0, fy) &
-                               pixel_coord(__ldg(xyz + 2), fZ, z0, fz);
+            const bool valid = pixel_coord(xyz[0], fW, x0, fx) &
+                               pixel_coord(xyz[1], fH, y0, fy) &
+                               pixel_coord(xyz[2], fZ, z0, fz);
             const bool vx[2] = {valid && x0 >= 0, valid && x0 < W - 1};
             const bool vy[2] = {y0 >= 0, y0 < H - 1};
             const bool vz[2] = {z0 >= 0, z0 < Z - 1};
@@ -202,10 +222,10 @@ bwd3d_generic(const __grid_constant__ Params p) {
             gz = group_sum<G>(gz);
             if (active) {
                 if (sub == 0) {
-                    p.grad_attn[s] = gA;
-                    p.grad_loc[3 * s] = any ? a * gx * fW : 0.f;
-                    p.grad_loc[3 * s + 1] = any ? a * gy * fH : 0.f;
-                    p.grad_loc[3 * s + 2] = any ? a * gz * fZ : 0.f;
+                    p.grad_attn[s] = gA;  // fused: grad_A, turned into d/d logits later
+                    p.grad_loc[3 * s] = any ? a * gx * eW : 0.f;
+                    p.grad_loc[3 * s + 1] = any ? a * gy * eH : 0.f;
+                    p.grad_loc[3 * s + 2] = any ? a * gz * eZ : 0.f;
                 }
                 float *dst = gl + r000 * rowf;
 #pragma unroll
@@ -245,7 +265,7 @@ __device__ __forceinline__ void add_global(float *dst, float wgt, const float (&
     for (int i = 0; i < N; i += 4)
         red_add_v4(dst + i, wgt * g[i], wgt * g[i + 1], wgt * g[i + 2], wgt * g[i + 3]);
 }
-template <int DT, int G, int NDIM, int LL, int PP, int BT>
+template <int DT, int G, int NDIM, int LL, int PP, int BT, bool FUSED>
 __global__ void __launch_bounds__(BT)
 bwd_tiled(const __grid_constant__ Params p) {
     constexpr int N = Vec<DT>::N;  // channels per lane (16 bytes of value)
@@ -278,6 +298,27 @@ bwd_tiled(const __grid_constant__ Params p) {
         const long long item = (b * p.Nq + q) * p.M + m;
         float g[N];
         unpack(ldg16(static_cast<const char *>(p.grad_out) + item * (rb / p.M) + sub * 16), g);
+        // fused: softmax weights of the samples this lane owns (max and sum over the group)
+        float av[NB];
+        if constexpr (FUSED) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int bt = 0; bt < NB; ++bt) {
+                const int own = bt * G + sub;
+                av[bt] = own < S ? __ldcs(p.attn + item * S + own) : -INFINITY;
+                mx = fmaxf(mx, av[bt]);
+            }
+            mx = group_max<G>(mx);
+            float sum = 0.f;
+#pragma unroll
+            for (int bt = 0; bt < NB; ++bt) {
+                av[bt] = bt * G + sub < S ? expf(av[bt] - mx) : 0.f;
+                sum += av[bt];
+            }
+            sum = group_sum<G>(sum);
+#pragma unroll
+            for (int bt = 0; bt < NB; ++bt) av[bt] = __fdiv_rn(av[bt], sum);
+        }
 
 #pragma unroll
         for (int bt = 0; bt < NB; ++bt) {
@@ -288,7 +329,15 @@ bwd_tiled(const __grid_constant__ Params p) {
             float xyz[NDIM];
 #pragma unroll
             for (int k = 0; k < NDIM; ++k) xyz[k] = __ldcs(p.loc + (item * S + so) * NDIM + k);
-            const float a = __ldcs(p.attn + item * S + so);
+            float a;
+            if constexpr (FUSED) {
+#pragma unroll
+                for (int k = 0; k < NDIM; ++k)
+                    xyz[k] = fused_location<NDIM>(p, item / p.M, so / PP, k, xyz[k]);
+                a = av[bt];
+            } else {
+                a = __ldcs(p.attn + item * S + so);
+            }
             Taps<NC> mine;
             float frac[NDIM];
             make_taps(p, so / PP, xyz, a, mine, frac);
@@ -348,10 +397,13 @@ bwd_tiled(const __grid_constant__ Params p) {
                 }
                 const bool any = mine.ok != 0u;
                 const int l = own / PP;
+                // fused: grad_A (turned into d/d logits later) and the offset gradient,
+                // d location / d offset = 1 / extent
                 p.grad_attn[s] = gA;
-                p.grad_loc[NDIM * s] = any ? a * gx * p.fW[l] : 0.f;
-                p.grad_loc[NDIM * s + 1] = any ? a * gy * p.fH[l] : 0.f;
-                if constexpr (NDIM == 3) p.grad_loc[NDIM * s + 2] = any ? a * gz * p.fZ[l] : 0.f;
+                p.grad_loc[NDIM * s] = any ? a * gx * (FUSED ? 1.f : p.fW[l]) : 0.f;
+                p.grad_loc[NDIM * s + 1] = any ? a * gy * (FUSED ? 1.f : p.fH[l]) : 0.f;
+                if constexpr (NDIM == 3)
+                    p.grad_loc[NDIM * s + 2] = any ? a * gz * (FUSED ? 1.f : p.fZ[l]) : 0.f;
             }
         }
     }
@@ -363,7 +415,7 @@ bwd_tiled(const __grid_constant__ Params p) {
 // slower).
 template <int NDIM> constexpr int bwd_block() { return NDIM == 3 ? 128 : 256; }
 
-template <int DT, int G, int NDIM, int LL, int PP>
+template <int DT, int G, int NDIM, int LL, int PP, bool FUSED>
 cudaError_t launch_bwd_tiled(Params p, cudaStream_t s) {
     constexpr int BT = bwd_block<NDIM>();
     // one round of lane groups per CTA: CTA = (b, m, run of BT / G queries)
@@ -371,27 +423,30 @@ cudaError_t launch_bwd_tiled(Params p, cudaStream_t s) {
     p.nchunk = static_cast<int>((p.Nq + p.qchunk - 1) / p.qchunk);
     const long long ctas = p.B * p.M * p.nchunk;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    bwd_tiled<DT, G, NDIM, LL, PP, BT><<<static_cast<unsigned>(ctas), BT, 0, s>>>(p);
+    bwd_tiled<DT, G, NDIM, LL, PP, BT, FUSED><<<static_cast<unsigned>(ctas), BT, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int DT, int G, int NDIM>
+template <int DT, int G, int NDIM, bool FUSED>
 cudaError_t backward_nd(const Params &p, cudaStream_t s) {
-    if (p.L == 4 && p.P == 4) return launch_bwd_tiled<DT, G, NDIM, 4, 4>(p, s);
-    if (p.L == 1 && p.P == 4) return launch_bwd_tiled<DT, G, NDIM, 1, 4>(p, s);
+    if (p.L == 4 && p.P == 4) return launch_bwd_tiled<DT, G, NDIM, 4, 4, FUSED>(p, s);
+    if (p.L == 1 && p.P == 4) return launch_bwd_tiled<DT, G, NDIM, 1, 4, FUSED>(p, s);
     const long long threads = p.n_items * G;
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>(blocks)), block(256);
-    if constexpr (NDIM == 2) bwd2d_generic<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
-    else bwd3d_generic<DT, G, 0, 0><<<grid, block, 0, s>>>(p);
+    if constexpr (NDIM == 2) bwd2d_generic<DT, G, 0, 0, FUSED><<<grid, block, 0, s>>>(p);
+    else bwd3d_generic<DT, G, 0, 0, FUSED><<<grid, block, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int NDIM>
+// FUSED: `loc` holds pixel offsets and `attn` logits (as in the fused forward); the
+// kernels write the offset gradients to grad_loc and grad_A to grad_attn, which
+// launch_fused_epilogue then turns into the logit gradients.
+template <int NDIM, bool FUSED>
 cudaError_t backward_dispatch(int dtype, int G, const Params &p, cudaStream_t s) {
 #define MSDA_BWD_CASE(DT, GG) \
-    if (dtype == DT && G == GG) return backward_nd<DT, GG, NDIM>(p, s);
+    if (dtype == DT && G == GG) return backward_nd<DT, GG, NDIM, FUSED>(p, s);
     MSDA_BWD_CASE(kF32, 1) MSDA_BWD_CASE(kF32, 2) MSDA_BWD_CASE(kF32, 4)
     MSDA_BWD_CASE(kF32, 8) MSDA_BWD_CASE(kF32, 16) MSDA_BWD_CASE(kF32, 32)
     MSDA_BWD_CASE(kBF16, 1) MSDA_BWD_CASE(kBF16, 2) MSDA_BWD_CASE(kBF16, 4)

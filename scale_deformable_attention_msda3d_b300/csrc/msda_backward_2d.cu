@@ -4,7 +4,7 @@
 namespace msda {
 
 cudaError_t launch_backward_2d(int dtype, int G, const Params &p, cudaStream_t s) {
-    return backward_dispatch<2>(dtype, G, p, s);
+    return backward_dispatch<2, false>(dtype, G, p, s);
 }
 
 }  // namespace msda

@@ -4,7 +4,7 @@
 namespace msda {
 
 cudaError_t launch_backward_3d(int dtype, int G, const Params &p, cudaStream_t s) {
-    return backward_dispatch<3>(dtype, G, p, s);
+    return backward_dispatch<3, false>(dtype, G, p, s);
 }
 
 }  // namespace msda

@@ -34,15 +34,6 @@ namespace msda {
 
 namespace {
 
-// Softmax statistics of an item's S logits (fused prologue, generic kernels): max and
-// the sum of expf(z - max).
-__device__ __forceinline__ void logit_stats(const float *z, int S, float &mx, float &sum) {
-    mx = -INFINITY;
-    for (int i = 0; i < S; ++i) mx = fmaxf(mx, __ldg(z + i));
-    sum = 0.f;
-    for (int i = 0; i < S; ++i) sum += expf(__ldg(z + i) - mx);
-}
-
 template <int DT, int G, int LL, int PP, bool FUSED>
 __global__ void __launch_bounds__(256)
 fwd2d_generic(const __grid_constant__ Params p) {

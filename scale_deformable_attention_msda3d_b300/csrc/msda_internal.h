@@ -29,6 +29,8 @@ struct Params {
     // sampled level and `attn` the attention logits; the location is ref[b, q, l] + offset /
     // extent and the weights are the softmax of the logits over the item's L * P samples
     const float *ref;           // [B, Nq, L, NDIM] reference points, or null
+    float *grad_ref;            // [B, Nq, L, NDIM] fused backward: reference-point gradient,
+                                // or null (not wanted)
     // sizes
     long long B, Nin, Nq;
     long long n_items;          // B * Nq * M work items (b, q, m)
@@ -48,6 +50,9 @@ struct Params {
 // Launchers: enqueue on `stream`, return the launch status.  dtype is kF32 / kBF16,
 // G = D * sizeof(dtype) / 16 lanes per work item.
 cudaError_t launch_forward(int ndim, int dtype, int G, const Params &p, cudaStream_t stream);
+// launch_backward: with p.ref set, the backward of the fused forward (loc = offsets,
+// attn = logits; grad_loc / grad_attn receive the offset and logit gradients, and
+// p.grad_ref, when set, the reference-point gradient).
 cudaError_t launch_backward(int ndim, int dtype, int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_zero_fill(float *ptr, long long n_floats, cudaStream_t stream);
 
@@ -58,6 +63,8 @@ cudaError_t launch_forward_bf16_2d(int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_forward_bf16_3d(int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_backward_2d(int dtype, int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_backward_3d(int dtype, int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_backward_fused_2d(int dtype, int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_backward_fused_3d(int dtype, int G, const Params &p, cudaStream_t stream);
 
 // Query order (msda_order.cu): sorts each batch's queries by the Morton code of the mean
 // of their sampling locations.  `hist` holds B * kOrderBuckets ints, `keys` B * Nq ints.

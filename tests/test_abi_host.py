@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert msda.msda_abi_version() == 10100
+    assert msda.msda_abi_version() == 10200
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -224,7 +224,38 @@ def test_fused_forward_rejects_bad_reference_points(lib):
         assert st == msda.MSDA_ERR_INVALID_ARG and msg in msda.msda_last_error()
     # the core's checks apply to the offsets / logits slots as to locations / weights
     st = msda.forward_fused_raw(2, dims(), FAKE, SH2, LS2, FAKE, 0, FAKE, FAKE, 0)
-    assert st == msda.MSDA_ERR_INVALID_ARG and "sampling_locations is NULL" in msda.msda_last_error()
+    assert st == msda.MSDA_ERR_INVALID_ARG and "sampling_offsets is NULL" in msda.msda_last_error()
+    st = msda.forward_fused_raw(2, dims(), FAKE, SH2, LS2, FAKE, FAKE, 0, FAKE, 0)
+    assert st == msda.MSDA_ERR_INVALID_ARG and "attention_logits is NULL" in msda.msda_last_error()
     st = msda.forward_fused_raw(3, dims(Nin=54), FAKE, SH3, LS3, FAKE, FAKE, FAKE, FAKE_MIS, 0)
     assert st == msda.MSDA_ERR_INVALID_ARG and "out is not 16-byte aligned" in msda.msda_last_error()
     assert msda.forward_fused_raw(2, dims(Nq=0), 0, SH2, LS2, 0, 0, 0, 0, 0) == msda.MSDA_OK
+
+
+def test_fused_backward_validates_before_any_launch(lib):
+    """Every pointer of msda{2,3}d_backward_fused is checked (NULL / 16-byte alignment)
+    before anything is enqueued; grad_reference_points may be NULL."""
+    args = dict(value=FAKE, ref=FAKE, off=FAKE, z=FAKE, go=FAKE, gv=FAKE, goff=FAKE, gz=FAKE,
+                gref=FAKE)
+    names = dict(value="value", ref="reference_points", off="sampling_offsets",
+                 z="attention_logits", go="grad_out", gv="grad_value",
+                 goff="grad_sampling_offsets", gz="grad_attention_logits",
+                 gref="grad_reference_points")
+
+    def call(nd, d, a):
+        sh, ls = (SH2, LS2) if nd == 2 else (SH3, LS3)
+        return msda.backward_fused_raw(nd, d, a["value"], sh, ls, a["ref"], a["off"], a["z"],
+                                       a["go"], a["gv"], a["goff"], a["gz"], a["gref"], 0)
+
+    for nd, d in ((2, dims()), (3, dims(Nin=54))):
+        for key, name in names.items():
+            bad = dict(args, **{key: FAKE_MIS})
+            st = call(nd, d, bad)
+            assert st == msda.MSDA_ERR_INVALID_ARG, (nd, key)
+            assert f"{name} is not 16-byte aligned" in msda.msda_last_error(), (nd, key)
+            if key == "gref":
+                continue
+            st = call(nd, d, dict(args, **{key: 0}))
+            assert st == msda.MSDA_ERR_INVALID_ARG and f"{name} is NULL" in msda.msda_last_error()
+    # nothing to do: B = 0 is OK without touching any pointer
+    assert call(2, dims(B=0), dict.fromkeys(args, 0)) == msda.MSDA_OK
