@@ -60,7 +60,8 @@ KERNEL_FILES = {
                 "msda_forward.cu", "msda_forward_f32_2d.cu", "msda_forward_f32_3d.cu",
                 "msda_forward_bf16_2d.cu", "msda_forward_bf16_3d.cu"),
     "backward": ("common.cuh", "msda_internal.h", "msda_abi.cpp", "msda_backward.cuh",
-                 "msda_backward.cu", "msda_backward_2d.cu", "msda_backward_3d.cu"),
+                 "msda_backward.cu", "msda_backward_2d.cu", "msda_backward_3d.cu",
+                 "msda_backward_fused_2d.cu", "msda_backward_fused_3d.cu"),
 }
 
 
@@ -367,6 +368,15 @@ def make_step(msda, w, inp, bufs, stream, ordered=False, prune=0.0, fused=False)
     (msda_query_order) and then runs the ordered forward, both inside the step.  With
     `prune` > 0 it runs the pruned forward (samples with |A| < prune skipped)."""
     shapes, starts = inp["spatial_shapes"], inp["level_start_index"]
+    if fused and w.backward:
+        fn = msda.msda2d_backward_fused if w.ndim == 2 else msda.msda3d_backward_fused
+
+        def step(i):
+            b = bufs[i % len(bufs)]
+            fn(b["value"], shapes, starts, b["ref"], b["loc"], b["attn"], b["grad_out"],
+               stream=stream, grad_value=b["gv"], grad_sampling_offsets=b["gl"],
+               grad_attention_logits=b["ga"], grad_reference_points=b["gref"])
+        return step, 4          # zero-fill, backward, logit and reference-point epilogues
     if fused:
         fn = msda.msda2d_forward_fused if w.ndim == 2 else msda.msda3d_forward_fused
 
@@ -410,9 +420,10 @@ def make_step(msda, w, inp, bufs, stream, ordered=False, prune=0.0, fused=False)
     return step, 2
 
 
-def cpu_baseline(w, inp, budget_s: float = 10.0):
+def cpu_baseline(w, inp, budget_s: float = 10.0, fused: bool = False):
     """The oracle as it stands (single-threaded C, double precision) on the full workload,
-    repeated until ~budget_s of CPU time; samples per second."""
+    repeated until ~budget_s of CPU time; samples per second.  `fused`: the oracle's fused
+    forward / backward on reference points, offsets and logits."""
     import oracle
     oracle.build()
     args = [np.ascontiguousarray(inp[k], dtype=np.float64) for k in
@@ -421,7 +432,13 @@ def cpu_baseline(w, inp, budget_s: float = 10.0):
     g = np.ascontiguousarray(inp["grad_out"], dtype=np.float64) if w.backward else None
     runs, t0 = 0, time.perf_counter()
     while True:
-        if w.backward:
+        if fused:
+            pro = (inp["reference_points"], inp["sampling_offsets"], inp["attention_logits"])
+            if w.backward:
+                oracle.backward_fused(w.ndim, args[0], shapes, starts, *pro, g)
+            else:
+                oracle.forward_fused(w.ndim, args[0], shapes, starts, *pro)
+        elif w.backward:
             oracle.backward(w.ndim, args[0], shapes, starts, args[1], args[2], g)
         else:
             oracle.forward(w.ndim, args[0], shapes, starts, args[1], args[2])
@@ -448,6 +465,9 @@ def run_ours(args):
         f = workloads.make_fused_inputs(w, seed=w.seed + rank)
         inp = dict(f, sampling_locations=f["sampling_offsets"],
                    attention_weights=f["attention_logits"])
+        if w.backward:  # the backward workload's upstream gradient
+            full = workloads.make_inputs(w, seed=w.seed + rank)
+            inp.update({k: full[k] for k in ("grad_out", "grad_out_bits") if k in full})
     else:
         inp = workloads.make_inputs(w, seed=w.seed + rank)
     base = to_device(inp, w, dev)
@@ -467,6 +487,8 @@ def run_ours(args):
             b["gv"] = torch.empty(b["value"].shape, dtype=torch.float32, device=dev)
             b["gl"] = torch.empty_like(b["loc"])
             b["ga"] = torch.empty_like(b["attn"])
+            if args.fused:
+                b["gref"] = torch.empty_like(b["ref"])
         if args.order:
             b["order"] = torch.empty((w.B, w.Nq), dtype=torch.int32, device=dev)
             b["ws"] = torch.empty(msda.query_order_workspace_bytes(
@@ -541,6 +563,9 @@ def run_ours(args):
         ref_b = inp["reference_points"].nbytes
         ab["total"] += ref_b
         ab["parts"]["reference_points"] = ref_b
+        if w.backward:
+            ab["total"] += ref_b
+            ab["parts"]["grad_reference_points"] = ref_b
     peak, peak_src = measured_peaks()
     per_launch_s = t_rank / args.steps
     achieved = ab["total"] / per_launch_s / 1e9
@@ -572,10 +597,12 @@ def run_ours(args):
                                  "note": "HBM3e nominal, the metric's ~8 TB/s"},
                      "algorithmic_bytes_per_launch": ab["total"],
                      "bytes_breakdown": ab["parts"],
-                     "kernel": ("zero-fill + msda bwd" if w.backward else
-                                "query order + ordered msda fwd" if args.order else
+                     "kernel": ("query order + ordered msda fwd" if args.order else
                                 "pruned msda fwd" if args.prune > 0 else
-                                "fused-prologue msda fwd" if args.fused else "msda fwd")},
+                                "fused-prologue msda fwd" if args.fused else "msda fwd")
+                               if not w.backward else
+                               ("zero-fill + fused-prologue msda bwd + epilogues" if args.fused
+                                else "zero-fill + msda bwd")},
         "warm_l2": {"ms_per_step": t_warm * 1e3 / n_warm,
                     "value": w.samples * n_warm / t_warm, "unit": UNIT, "steps": n_warm,
                     "note": "rank 0; one input set back to back, outside the timed region"},
@@ -586,7 +613,7 @@ def run_ours(args):
     if e2e is not None:
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, inp, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(w, inp, budget_s=args.cpu_budget, fused=args.fused)
     barrier(world)
     return line
 
@@ -760,8 +787,9 @@ def main(argv=None):
                     help="forward workloads: compute the locality-aware query order inside "
                          "each step and run the ordered forward")
     ap.add_argument("--fused", action="store_true",
-                    help="forward workloads: reference points, pixel offsets and logits in; "
-                         "the kernel forms locations and the softmax (no e2e leg)")
+                    help="reference points, pixel offsets and logits in; the kernel forms "
+                         "locations and the softmax (backward workloads: the fused backward, "
+                         "with offset, logit and reference-point gradients; no e2e leg)")
     ap.add_argument("--prune", type=float, default=0.0,
                     help="forward workloads: skip samples with |A| below this threshold "
                          "(approximate; 0 = exact)")
@@ -777,8 +805,6 @@ def main(argv=None):
         ap.error("--order and --prune apply to the forward workloads")
     if sum([bool(args.order), args.prune > 0, bool(args.fused)]) > 1:
         ap.error("--order, --prune and --fused are separate modes")
-    if args.fused and workloads.WORKLOADS[args.workload].backward:
-        ap.error("--fused applies to the forward workloads")
     if args.fused:
         args.no_e2e = True
     line = run_reference(args) if args.impl == "reference" else run_ours(args)

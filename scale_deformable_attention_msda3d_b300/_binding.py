@@ -491,7 +491,8 @@ def msda3d_forward_fused(value, spatial_shapes, level_start_index, reference_poi
 
 def _backward_fused(ndim, value, spatial_shapes, level_start_index, reference_points,
                     sampling_offsets, attention_logits, grad_out, need_reference_grad=True,
-                    stream=None):
+                    stream=None, grad_value=None, grad_sampling_offsets=None,
+                    grad_attention_logits=None, grad_reference_points=None):
     torch = _torch()
     dims = _dims_from(value, sampling_offsets, ndim)
     _require(value, "value")
@@ -506,10 +507,20 @@ def _backward_fused(ndim, value, spatial_shapes, level_start_index, reference_po
     if tuple(grad_out.shape) != (dims.B, dims.Nq, dims.M * dims.D):
         raise MsdaError(MSDA_ERR_INVALID_ARG, "grad_out must be [B, Nq, M*D]")
     dev = value.device
-    grad_value = torch.empty(value.shape, dtype=torch.float32, device=dev)
-    grad_off = torch.empty_like(sampling_offsets)
-    grad_logits = torch.empty_like(attention_logits)
-    grad_ref = torch.empty_like(reference_points) if need_reference_grad else None
+    if grad_value is None:
+        grad_value = torch.empty(value.shape, dtype=torch.float32, device=dev)
+    grad_off = (torch.empty_like(sampling_offsets) if grad_sampling_offsets is None
+                else grad_sampling_offsets)
+    grad_logits = (torch.empty_like(attention_logits) if grad_attention_logits is None
+                   else grad_attention_logits)
+    grad_ref = None
+    if need_reference_grad:
+        grad_ref = (torch.empty_like(reference_points) if grad_reference_points is None
+                    else grad_reference_points)
+        _require(grad_ref, "grad_reference_points", torch.float32)
+    _require(grad_value, "grad_value", torch.float32)
+    _require(grad_off, "grad_sampling_offsets", torch.float32)
+    _require(grad_logits, "grad_attention_logits", torch.float32)
     lib = load()
     st = backward_fused_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
                             reference_points.data_ptr(), sampling_offsets.data_ptr(),
@@ -523,22 +534,23 @@ def _backward_fused(ndim, value, spatial_shapes, level_start_index, reference_po
 
 def msda2d_backward_fused(value, spatial_shapes, level_start_index, reference_points,
                           sampling_offsets, attention_logits, grad_out, need_reference_grad=True,
-                          stream=None):
+                          stream=None, **outs):
     """Backward of msda2d_forward_fused.  Returns (grad_value fp32, grad_sampling_offsets,
     grad_attention_logits, grad_reference_points or None when need_reference_grad is
-    False)."""
+    False).  Output tensors may be passed in as grad_value=, grad_sampling_offsets=,
+    grad_attention_logits=, grad_reference_points=."""
     return _backward_fused(2, value, spatial_shapes, level_start_index, reference_points,
                            sampling_offsets, attention_logits, grad_out, need_reference_grad,
-                           stream)
+                           stream, **outs)
 
 
 def msda3d_backward_fused(value, spatial_shapes, level_start_index, reference_points,
                           sampling_offsets, attention_logits, grad_out, need_reference_grad=True,
-                          stream=None):
+                          stream=None, **outs):
     """Backward of msda3d_forward_fused (see msda2d_backward_fused)."""
     return _backward_fused(3, value, spatial_shapes, level_start_index, reference_points,
                            sampling_offsets, attention_logits, grad_out, need_reference_grad,
-                           stream)
+                           stream, **outs)
 
 
 def msda2d_forward_pruned(value, spatial_shapes, level_start_index, sampling_locations,
