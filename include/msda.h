@@ -177,8 +177,9 @@ msda_status msda3d_forward_fused(const msda_dims *dims, const void *value,
  *                                                reference points need no gradient
  * grad_value is zero-filled by the call and accumulated with fp32 atomics, as in
  * msda2d_backward.  The locations and weights are formed exactly as the fused forward
- * forms them; the logit gradients are finished by a second small kernel on the same
- * stream and the reference-point gradients (a sum in the order m, p) by a third.  All
+ * forms them.  The backward kernel forms the logit gradients itself for the compiled
+ * (L, P) pairs, and a second small kernel on the same stream forms them for the others;
+ * the reference-point gradients (a sum in the order m, p) come from one more.  All
  * other arguments, limits and errors are those of msda2d_backward / msda3d_backward and
  * msda2d_forward_fused.
  */

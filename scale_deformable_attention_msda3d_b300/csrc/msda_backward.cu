@@ -1,7 +1,7 @@
 // Backward entry of the kernel layer: the grad_value zero-fill, the dispatch to the 2D or
 // 3D instantiation (msda_backward_{2d,3d}.cu, fused prologue msda_backward_fused_{2d,3d}.cu;
-// kernels in msda_backward.cuh) and the two small kernels that finish the fused backward's
-// logit and reference-point gradients.
+// kernels in msda_backward.cuh) and the two small kernels that finish the fused backward:
+// the logit gradients after the generic kernels, and the reference-point gradients.
 #include "common.cuh"
 
 namespace msda {
@@ -15,24 +15,32 @@ __global__ void zero_fill_kernel(float4 *__restrict__ p, long long n4) {
         p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// Fused backward, logit gradients: the kernels left grad_A in grad_attn; with the item's
-// softmax weights A (recomputed from the logits as the kernels formed them),
+// Fused backward through the generic kernels, logit gradients: those kernels leave grad_A
+// in grad_attn; with the item's softmax weights A (recomputed from the logits),
 //   d/d logit_s = A_s * (grad_A_s - sum_t A_t * grad_A_t)
-// (softmax Jacobian).  One thread per (b, q, m) item, in place.
+// (softmax Jacobian), in place.  T lanes (a power of two, T <= 32) per (b, q, m) item; lane
+// j takes samples j, j + T, ..., so a warp reads whole runs of consecutive items.
 __global__ void logit_grad_kernel(const float *__restrict__ logits, float *grad, long long n_items,
-                                  int S) {
-    const long long item = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (item >= n_items) return;
+                                  int S, int T) {
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if ((t & ~31LL) / T >= n_items) return;  // whole warps leave together (shuffles below)
+    long long item = t / T;
+    const bool active = item < n_items;
+    if (!active) item = n_items - 1;
+    const int j = static_cast<int>(t % T);
     const float *z = logits + item * S;
     float *g = grad + item * S;
-    float mx, sum;
-    logit_stats(z, S, mx, sum);
+    float mx = -INFINITY;
+    for (int s = j; s < S; s += T) mx = fmaxf(mx, __ldg(z + s));
+    for (int o = T / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o, T));
+    float sum = 0.f;
+    for (int s = j; s < S; s += T) sum += expf(__ldg(z + s) - mx);
+    for (int o = T / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o, T);
     float dot = 0.f;
-    for (int s = 0; s < S; ++s) dot = fmaf(__fdiv_rn(expf(__ldg(z + s) - mx), sum), g[s], dot);
-    for (int s = 0; s < S; ++s) {
-        const float a = __fdiv_rn(expf(__ldg(z + s) - mx), sum);
-        g[s] = a * (g[s] - dot);
-    }
+    for (int s = j; s < S; s += T) dot = fmaf(__fdiv_rn(expf(__ldg(z + s) - mx), sum), g[s], dot);
+    for (int o = T / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o, T);
+    if (!active) return;
+    for (int s = j; s < S; s += T) g[s] = __fdiv_rn(expf(__ldg(z + s) - mx), sum) * (g[s] - dot);
 }
 
 // Fused backward, reference-point gradients: location = ref + offset / extent, so
@@ -56,13 +64,18 @@ __global__ void ref_grad_kernel(const __grid_constant__ Params p, int ndim) {
 
 cudaError_t launch_fused_epilogue(int ndim, const Params &p, cudaStream_t s) {
     const int S = p.L * p.P;
-    const long long blocks = (p.n_items + 255) / 256;
     const long long n = p.B * p.Nq * p.L * ndim;
-    if (blocks > 0x7fffffffLL || (n + 255) / 256 > 0x7fffffffLL)
-        return cudaErrorInvalidConfiguration;
-    logit_grad_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p.attn, p.grad_attn,
-                                                                     p.n_items, S);
-    cudaError_t e = cudaGetLastError();
+    if ((n + 255) / 256 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaSuccess;
+    if (!backward_is_tiled(p)) {  // bwd_tiled formed the logit gradients itself
+        int T = 1;
+        while (T < 32 && T < S) T <<= 1;
+        const long long blocks = (p.n_items * T + 255) / 256;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        logit_grad_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p.attn, p.grad_attn,
+                                                                         p.n_items, S, T);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess || p.grad_ref == nullptr) return e;
     ref_grad_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(p, ndim);
     return cudaGetLastError();

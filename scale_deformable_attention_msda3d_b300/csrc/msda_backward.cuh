@@ -266,8 +266,7 @@ __device__ __forceinline__ void add_global(float *dst, float wgt, const float (&
         red_add_v4(dst + i, wgt * g[i], wgt * g[i + 1], wgt * g[i + 2], wgt * g[i + 3]);
 }
 template <int DT, int G, int NDIM, int LL, int PP, int BT, bool FUSED>
-__global__ void __launch_bounds__(BT)
-bwd_tiled(const __grid_constant__ Params p) {
+__device__ __forceinline__ void bwd_tiled_body(const Params &p) {
     constexpr int N = Vec<DT>::N;  // channels per lane (16 bytes of value)
     constexpr int NC = 1 << NDIM;
     constexpr int S = LL * PP;
@@ -299,7 +298,10 @@ bwd_tiled(const __grid_constant__ Params p) {
         float g[N];
         unpack(ldg16(static_cast<const char *>(p.grad_out) + item * (rb / p.M) + sub * 16), g);
         // fused: softmax weights of the samples this lane owns (max and sum over the group)
-        float av[NB];
+        // and their grad_A, kept until the item's logit gradients can be formed
+        float av[NB], gAs[NB];
+#pragma unroll
+        for (int bt = 0; bt < NB; ++bt) gAs[bt] = 0.f;
         if constexpr (FUSED) {
             float mx = -INFINITY;
 #pragma unroll
@@ -397,17 +399,51 @@ bwd_tiled(const __grid_constant__ Params p) {
                 }
                 const bool any = mine.ok != 0u;
                 const int l = own / PP;
-                // fused: grad_A (turned into d/d logits later) and the offset gradient,
-                // d location / d offset = 1 / extent
-                p.grad_attn[s] = gA;
+                // fused: the offset gradient, d location / d offset = 1 / extent
+                if constexpr (FUSED) gAs[bt] = gA;
+                else p.grad_attn[s] = gA;
                 p.grad_loc[NDIM * s] = any ? a * gx * (FUSED ? 1.f : p.fW[l]) : 0.f;
                 p.grad_loc[NDIM * s + 1] = any ? a * gy * (FUSED ? 1.f : p.fH[l]) : 0.f;
                 if constexpr (NDIM == 3)
                     p.grad_loc[NDIM * s + 2] = any ? a * gz * (FUSED ? 1.f : p.fZ[l]) : 0.f;
             }
         }
+        if constexpr (FUSED) {
+            // logit gradients (softmax Jacobian): A_s * (grad_A_s - sum_t A_t * grad_A_t)
+            float dot = 0.f;
+#pragma unroll
+            for (int bt = 0; bt < NB; ++bt)
+                if (bt * G + sub < S) dot = fmaf(av[bt], gAs[bt], dot);
+            dot = group_sum<G>(dot);
+            if (active) {
+#pragma unroll
+                for (int bt = 0; bt < NB; ++bt) {
+                    const int own = bt * G + sub;
+                    if (own < S) p.grad_attn[item * S + own] = av[bt] * (gAs[bt] - dot);
+                }
+            }
+        }
     }
 
+}
+
+// Resident blocks per SM asked of the compiler for rows of up to 8 lanes: 3 x 256 threads
+// in 2D (at most 85 registers) and 4 x 128 in 3D (at most 128).  Measured on B300 against
+// no bound: the encoder backward 407 us against 425 us, the volume one 984 against 1000,
+// and the fused encoder backward 456 against 508 (its prologue would otherwise cost a
+// block per SM).  Wider rows (bwd_tiled_wide) keep the compiler's own choice.
+template <int NDIM> constexpr int bwd_min_blocks() { return NDIM == 2 ? 3 : 4; }
+
+template <int DT, int G, int NDIM, int LL, int PP, int BT, bool FUSED>
+__global__ void __launch_bounds__(BT, (bwd_min_blocks<NDIM>()))
+bwd_tiled(const __grid_constant__ Params p) {
+    bwd_tiled_body<DT, G, NDIM, LL, PP, BT, FUSED>(p);
+}
+
+template <int DT, int G, int NDIM, int LL, int PP, int BT, bool FUSED>
+__global__ void __launch_bounds__(BT)
+bwd_tiled_wide(const __grid_constant__ Params p) {
+    bwd_tiled_body<DT, G, NDIM, LL, PP, BT, FUSED>(p);
 }
 
 // Block size of the tiled backward: 256 threads in 2D, 128 in 3D (measured on B300: the
@@ -423,14 +459,20 @@ cudaError_t launch_bwd_tiled(Params p, cudaStream_t s) {
     p.nchunk = static_cast<int>((p.Nq + p.qchunk - 1) / p.qchunk);
     const long long ctas = p.B * p.M * p.nchunk;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    bwd_tiled<DT, G, NDIM, LL, PP, BT, FUSED><<<static_cast<unsigned>(ctas), BT, 0, s>>>(p);
+    if constexpr (G <= 8)
+        bwd_tiled<DT, G, NDIM, LL, PP, BT, FUSED><<<static_cast<unsigned>(ctas), BT, 0, s>>>(p);
+    else
+        bwd_tiled_wide<DT, G, NDIM, LL, PP, BT, FUSED>
+            <<<static_cast<unsigned>(ctas), BT, 0, s>>>(p);
     return cudaGetLastError();
 }
 
 template <int DT, int G, int NDIM, bool FUSED>
 cudaError_t backward_nd(const Params &p, cudaStream_t s) {
-    if (p.L == 4 && p.P == 4) return launch_bwd_tiled<DT, G, NDIM, 4, 4, FUSED>(p, s);
-    if (p.L == 1 && p.P == 4) return launch_bwd_tiled<DT, G, NDIM, 1, 4, FUSED>(p, s);
+    if (backward_is_tiled(p)) {
+        if (p.L == 4) return launch_bwd_tiled<DT, G, NDIM, 4, 4, FUSED>(p, s);
+        return launch_bwd_tiled<DT, G, NDIM, 1, 4, FUSED>(p, s);
+    }
     const long long threads = p.n_items * G;
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -441,8 +483,9 @@ cudaError_t backward_nd(const Params &p, cudaStream_t s) {
 }
 
 // FUSED: `loc` holds pixel offsets and `attn` logits (as in the fused forward); the
-// kernels write the offset gradients to grad_loc and grad_A to grad_attn, which
-// launch_fused_epilogue then turns into the logit gradients.
+// kernels write the offset gradients to grad_loc.  bwd_tiled writes the logit gradients
+// itself; the generic kernels write grad_A to grad_attn, which the epilogue in
+// msda_backward.cu turns into the logit gradients.
 template <int NDIM, bool FUSED>
 cudaError_t backward_dispatch(int dtype, int G, const Params &p, cudaStream_t s) {
 #define MSDA_BWD_CASE(DT, GG) \

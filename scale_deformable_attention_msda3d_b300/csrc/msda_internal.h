@@ -47,6 +47,9 @@ struct Params {
     int nchunk, qchunk;
 };
 
+// (L, P) pairs with a compiled backward (bwd_tiled); others take the generic kernels.
+inline bool backward_is_tiled(const Params &p) { return p.P == 4 && (p.L == 4 || p.L == 1); }
+
 // Launchers: enqueue on `stream`, return the launch status.  dtype is kF32 / kBF16,
 // G = D * sizeof(dtype) / 16 lanes per work item.
 cudaError_t launch_forward(int ndim, int dtype, int G, const Params &p, cudaStream_t stream);
