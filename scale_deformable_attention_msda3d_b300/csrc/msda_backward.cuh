@@ -9,8 +9,9 @@
 //   grad_x (px)   = a * sum_c dw_c/dx <g, v_c>,   grad_loc_x = W_l * grad_x   (x = loc*W - 0.5)
 //   grad_value[c] += a * w_c * g                  (corners inside the level only)
 //
-// Two kernels:
-// * bwd_tiled (the compiled (L, P) pairs).  A CTA handles one (batch, head) and a run of
+// Kernels:
+// * bwd_tiled / bwd_tiled_wide (the compiled (L, P) pairs; the same body, rows of up to 8
+//   lanes / wider rows, which differ only in the residency they ask of the compiler).  A CTA handles one (batch, head) and a run of
 //   queries; a lane group of G lanes (16 bytes of channels each) handles one query.  Lane
 //   j of the group owns samples j, G + j, 2G + j, ...: it reads their locations and
 //   weights and computes their taps, which the group takes by shuffle.  Every lane forms
@@ -21,6 +22,10 @@
 //   part shared-memory fp32 atomics ran about ten times slower than the L2 reductions.)
 // * bwd{2,3}d_generic (any L, P): every lane of the group computes every sample, reduces
 //   grad_A / grad_loc with xor shuffles and scatters with red.global.add.v4.f32.
+// With FUSED (the backward of the fused-prologue forward) the kernels form the locations
+// and softmax weights from reference points, offsets and logits as the fused forward does,
+// and write offset gradients (d location / d offset = 1 / extent); bwd_tiled also forms
+// the logit gradients, the generic kernels leave grad_A for an epilogue.
 #pragma once
 
 #include "common.cuh"
