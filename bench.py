@@ -376,7 +376,10 @@ def make_step(msda, w, inp, bufs, stream, ordered=False, prune=0.0, fused=False)
             fn(b["value"], shapes, starts, b["ref"], b["loc"], b["attn"], b["grad_out"],
                stream=stream, grad_value=b["gv"], grad_sampling_offsets=b["gl"],
                grad_attention_logits=b["ga"], grad_reference_points=b["gref"])
-        return step, 4          # zero-fill, backward, logit and reference-point epilogues
+        # zero-fill, backward, reference-point epilogue (+ the logit epilogue when the
+        # generic kernels run, i.e. (L, P) outside the compiled pairs)
+        tiled = w.P == 4 and w.L in (1, 4)
+        return step, 3 if tiled else 4
     if fused:
         fn = msda.msda2d_forward_fused if w.ndim == 2 else msda.msda3d_forward_fused
 
