@@ -433,10 +433,11 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
 }
 
 // Resident blocks per SM asked of the compiler for rows of up to 8 lanes: 3 x 256 threads
-// in 2D (at most 85 registers) and 4 x 128 in 3D (at most 128).  Measured on B300 against
-// no bound: the encoder backward 407 us against 425 us, the volume one 984 against 1000,
-// and the fused encoder backward 456 against 508 (its prologue would otherwise cost a
-// block per SM).  Wider rows (bwd_tiled_wide) keep the compiler's own choice.
+// in 2D (at most 85 registers) and 4 x 128 in 3D (at most 128).  The plain kernels reach
+// that residency without the bound, but are scheduled better under it; the fused 2D kernel
+// would otherwise take 86 registers and lose a block.  Measured on B300 against no bound:
+// the encoder backward 407 us against 425 us, the volume one 984 against 1000, the fused
+// encoder backward 456 against 508.  Wider rows (bwd_tiled_wide) keep the compiler's choice.
 template <int NDIM> constexpr int bwd_min_blocks() { return NDIM == 2 ? 3 : 4; }
 
 template <int DT, int G, int NDIM, int LL, int PP, int BT, bool FUSED>
