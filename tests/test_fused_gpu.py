@@ -131,7 +131,7 @@ def _check_bwd(msda, nd, f, w, what):
     loc = oracle.fused_locations(f["spatial_shapes"], f["reference_points"],
                                  f["sampling_offsets"])
     a = oracle.softmax_weights(f["attention_logits"])
-    mag_v, mag_l, _ = oracle.backward(*args, loc, a, np.abs(g))
+    mag_v, _, _ = oracle.backward(*args, loc, a, np.abs(g))
     _, gl_abs, _ = oracle.backward(*args, loc, a, g)
     vt = "f32" if w.dtype == "f32" else "bf16"
     check(gv, rgv, vt, what + " grad_value", mag_v)

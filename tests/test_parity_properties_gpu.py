@@ -7,7 +7,9 @@ half of the pixel coordinates are moved onto the places where the sampling rule 
 pixel centres (a corner weight is exactly 0 or 1), the zero-padding boundaries -1 and
 extent (the sample just stops contributing), and the half-pixel bands next to them (only
 some corners exist).  Forward and backward must match the oracle within the fp32 / bf16
-tolerances of ``gpu_parity``.  Runs are derandomised, so a failure reproduces.
+tolerances of ``gpu_parity``.  A second test draws fused-prologue problems (reference
+points, offsets, logits) and checks the fused forward and backward against the oracle's
+fused composition.  Runs are derandomised, so a failure reproduces.
 """
 from __future__ import annotations
 
@@ -18,8 +20,9 @@ hypothesis = pytest.importorskip("hypothesis")
 from hypothesis import HealthCheck, given, settings  # noqa: E402
 from hypothesis import strategies as st  # noqa: E402
 
+import oracle  # noqa: E402
 import workloads  # noqa: E402
-from gpu_parity import check_backward, check_forward  # noqa: E402
+from gpu_parity import check, check_backward, check_forward, host  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -83,3 +86,64 @@ def test_drawn_problems_forward_and_backward(msda, problem):
     nd, dtype, inp = problem
     check_forward(msda, nd, inp, dtype, "drawn fwd")
     check_backward(msda, nd, inp, dtype, "drawn bwd")
+
+
+@st.composite
+def fused_problems(draw):
+    nd = draw(st.sampled_from([2, 3]))
+    dtype = draw(st.sampled_from(["f32", "bf16"]))
+    row_bytes = draw(st.sampled_from([16, 32, 64, 128]))
+    D = row_bytes // (4 if dtype == "f32" else 2)
+    L, P = draw(st.sampled_from([(4, 4), (1, 4), (2, 3), (3, 1)]))
+    top = 9 if nd == 2 else 5
+    shapes = tuple(tuple(draw(st.integers(1, top)) for _ in range(nd)) for _ in range(L))
+    B, Nq, M = draw(st.integers(1, 2)), draw(st.integers(1, 60)), draw(st.integers(1, 4))
+    seed = draw(st.integers(0, 2**31 - 1))
+    w = workloads.Workload("drawn", nd, B, shapes, Nq, M, D, P, dtype, seed % 100000,
+                           query_layout="uniform", offset_std_px=draw(st.sampled_from([0.5, 3.0])))
+    f = workloads.make_fused_inputs(w)
+    rng = np.random.default_rng(seed)
+    # some items with far-apart logits, some references outside [0, 1]
+    f["attention_logits"] *= rng.choice([1.0, 6.0], size=f["attention_logits"].shape[:3])[..., None, None]
+    f["reference_points"] += rng.choice([0.0, 0.6, -0.6], size=f["reference_points"].shape).astype(np.float32)
+    g = rng.standard_normal((B, Nq, M * D), dtype=np.float32)
+    bits = None
+    if dtype == "bf16":
+        bits = workloads.f32_to_bf16_bits(g)
+        g = workloads.bf16_bits_to_f32(bits)
+    return nd, dtype, f, g, bits
+
+
+@SETTINGS
+@given(fused_problems())
+def test_drawn_fused_problems_forward_and_backward(msda, problem):
+    """The fused-prologue forward and backward on drawn problems, compiled and generic
+    (L, P) pairs, against oracle.forward_fused / oracle.backward_fused."""
+    import torch
+    nd, dtype, f, g, bits = problem
+    dev = torch.device("cuda", 0)
+    value = (torch.from_numpy(f["value_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+             if dtype == "bf16" else torch.from_numpy(f["value"]).to(dev))
+    ref = torch.from_numpy(f["reference_points"]).to(dev)
+    off = torch.from_numpy(f["sampling_offsets"]).to(dev)
+    z = torch.from_numpy(f["attention_logits"]).to(dev)
+    go = (torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16) if dtype == "bf16"
+          else torch.from_numpy(g).to(dev))
+    sh, ls = f["spatial_shapes"], f["level_start_index"]
+    fwd = msda.msda2d_forward_fused if nd == 2 else msda.msda3d_forward_fused
+    bwd = msda.msda2d_backward_fused if nd == 2 else msda.msda3d_backward_fused
+    out = fwd(value, sh, ls, ref, off, z)
+    gv, goff, gz, gref = bwd(value, sh, ls, ref, off, z, go)
+    torch.cuda.synchronize()
+    args = (nd, f["value"], sh, ls)
+    pro = (f["reference_points"], f["sampling_offsets"], f["attention_logits"])
+    check(host(out), oracle.forward_fused(*args, *pro), dtype, "drawn fused fwd")
+    rgv, rgoff, rgz, rgref = oracle.backward_fused(*args, *pro, g)
+    loc = oracle.fused_locations(sh, f["reference_points"], f["sampling_offsets"])
+    a = oracle.softmax_weights(f["attention_logits"])
+    mag_v, _, _ = oracle.backward(*args, loc, a, np.abs(g))
+    _, gl, _ = oracle.backward(*args, loc, a, g)
+    check(host(gv), rgv, "f32" if dtype == "f32" else "bf16", "drawn fused grad_value", mag_v)
+    check(host(goff), rgoff, dtype, "drawn fused grad_offsets")
+    check(host(gz), rgz, dtype, "drawn fused grad_logits")
+    check(host(gref), rgref, dtype, "drawn fused grad_ref", np.abs(gl).sum(axis=(2, 4)))
