@@ -742,9 +742,21 @@ def run_reference(args):
     attn = np.ascontiguousarray(inp["attention_weights"][:1], dtype=np.float64)
     g = (np.ascontiguousarray(inp["grad_out"][:1], dtype=np.float64) if w.backward else None)
 
+    if args.fused:
+        # the fused prologue's inputs: reference points, pixel offsets and logits
+        f = workloads.make_fused_inputs(w)
+        ref, off, z = (f["reference_points"][:1], f["sampling_offsets"][:1],
+                       f["attention_logits"][:1])
+        value = np.ascontiguousarray(f["value"][:1], dtype=np.float64)
+
     def run(q0, q1):
         sl = slice(q0, q1)
-        if w.backward:
+        if args.fused and w.backward:
+            oracle.backward_fused(w.ndim, value, shapes, starts, ref[:, sl], off[:, sl],
+                                  z[:, sl], g[:, sl])
+        elif args.fused:
+            oracle.forward_fused(w.ndim, value, shapes, starts, ref[:, sl], off[:, sl], z[:, sl])
+        elif w.backward:
             oracle.backward(w.ndim, value, shapes, starts, loc[:, sl], attn[:, sl], g[:, sl])
         else:
             oracle.forward(w.ndim, value, shapes, starts, loc[:, sl], attn[:, sl])
@@ -766,7 +778,8 @@ def run_reference(args):
     el = time.perf_counter() - t0
     v = nq * per_q * args.steps / el
     sample = (f"each step: queries [q0, q0+{nq}) of batch 0 of the {w.name} workload "
-              f"({nq * per_q} samples), all heads/levels/points; 1 thread, fp64 oracle")
+              f"({nq * per_q} samples), all heads/levels/points; 1 thread, fp64 oracle"
+              + ("; fused prologue (reference points, offsets, logits)" if args.fused else ""))
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
