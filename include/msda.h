@@ -47,7 +47,9 @@
  * last non-OK status returned on the calling thread.
  *
  * Limits: 1 <= L <= MSDA_MAX_LEVELS, 1 <= P <= MSDA_MAX_POINTS, Nin <= 2^30, every level
- * extent in [1, 2^24) and every level at most 2^30 pixels, M * D * sizeof(value dtype)
+ * extent in [1, 2^23) (an extent of 2^23 or more returns MSDA_ERR_UNSUPPORTED: the pixel
+ * coordinate loc * extent - 0.5 is formed exactly in fp32, which needs the product below
+ * 2^23) and every level at most 2^30 pixels, M * D * sizeof(value dtype)
  * below 2^31 bytes; D * sizeof(value dtype) must be 16, 32, 64, 128, 256 or 512 bytes
  * (fp32: D in {4, 8, 16, 32, 64, 128}; bf16: D in {8, 16, 32, 64, 128, 256}); every
  * pointer must be 16-byte aligned.  B == 0 or Nq == 0 is a valid empty call (the

@@ -66,7 +66,10 @@ __device__ __forceinline__ uint4 pack(const float (&v)[8]) {
 //   Rounding x itself to fp32 would also cost up to ~8e-6 px of accuracy at extent 150.
 //
 // Intrinsics with explicit rounding keep the compiler from contracting the product and
-// the subtraction into one FMA, which would lose the error term.
+// the subtraction into one FMA, which would lose the error term.  The subtraction of 0.5
+// is exact while |loc * extent| < 2^23 (the fp32 spacing there is at most 0.5); the ABI
+// caps extents below 2^23, and a product beyond that belongs to a sample outside the level
+// whichever way the subtraction rounds.
 //
 // A coordinate that is not finite or lies at or beyond -1 / the extent is reported as
 // invalid (the function returns false; i0 = -2 and frac = 0 so no weight is NaN).  The

@@ -68,10 +68,15 @@ msda_status build_params(const msda_dims *d, int ndim, const int64_t *shapes,
         int64_t size = 1;
         for (int k = 0; k < ndim; ++k) {
             const int64_t e = shapes[l * ndim + k];
-            if (e < 1 || e >= (int64_t(1) << 24))
-                return fail(MSDA_ERR_INVALID_ARG,
-                            "spatial_shapes[%d][%d] = %lld must be in [1, 2^24)", l, k,
-                            (long long)e);
+            if (e < 1)
+                return fail(MSDA_ERR_INVALID_ARG, "spatial_shapes[%d][%d] = %lld must be >= 1",
+                            l, k, (long long)e);
+            // the kernels form loc * extent - 0.5 exactly in fp32 (product error by FMA, the
+            // subtraction exact), which holds while the product stays below 2^23
+            if (e >= (int64_t(1) << 23))
+                return fail(MSDA_ERR_UNSUPPORTED,
+                            "spatial_shapes[%d][%d] = %lld: extents of 2^23 pixels or more "
+                            "are not supported", l, k, (long long)e);
             if (!mul_ok(size, e, &size) || size > (int64_t(1) << 30))
                 return fail(MSDA_ERR_INVALID_ARG, "level %d has too many pixels", l);
         }

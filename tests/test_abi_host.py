@@ -116,8 +116,9 @@ def test_forward_rejects_bad_arguments(lib, case, status, msg):
 def test_forward_3d_rejects_bad_arguments(lib):
     assert fwd(nd=3, d=dims(Nin=54), sh=np.array([[2, 4, 6], [1, 2, 4]])) == \
         msda.MSDA_ERR_INVALID_ARG
+    # an extent of 2^23 or more is outside what the kernels support
     assert fwd(nd=3, d=dims(Nin=54), sh=np.array([[2, 4, 2 ** 24], [1, 2, 3]])) == \
-        msda.MSDA_ERR_INVALID_ARG
+        msda.MSDA_ERR_UNSUPPORTED
 
 
 def test_null_metadata_and_dims(lib):
@@ -259,3 +260,18 @@ def test_fused_backward_validates_before_any_launch(lib):
             assert st == msda.MSDA_ERR_INVALID_ARG and f"{name} is NULL" in msda.msda_last_error()
     # nothing to do: B = 0 is OK without touching any pointer
     assert call(2, dims(B=0), dict.fromkeys(args, 0)) == msda.MSDA_OK
+
+
+def test_extents_of_2_23_or_more_are_unsupported(lib):
+    """Extents up to 2^23 - 1 pass validation (the call then stops at the NULL value
+    pointer, before any launch); 2^23 returns MSDA_ERR_UNSUPPORTED."""
+    big = (1 << 23) - 1
+    for nd, sh in ((2, np.array([[1, big]])), (3, np.array([[big, 1, 1]]))):
+        d = msda.make_dims(1, big, 4, 1, 4, 1, 4, msda.MSDA_F32)
+        st = msda.forward_raw(nd, d, 0, sh, np.array([0]), FAKE, FAKE, FAKE, 0)
+        assert st == msda.MSDA_ERR_INVALID_ARG and "value is NULL" in msda.msda_last_error()
+        sh2 = sh.copy()
+        sh2[sh2 == big] = big + 1
+        d2 = msda.make_dims(1, big + 1, 4, 1, 4, 1, 4, msda.MSDA_F32)
+        st = msda.forward_raw(nd, d2, FAKE, sh2, np.array([0]), FAKE, FAKE, FAKE, 0)
+        assert st == msda.MSDA_ERR_UNSUPPORTED and "2^23" in msda.msda_last_error()

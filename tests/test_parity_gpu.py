@@ -139,6 +139,19 @@ def test_maximum_channels(msda):
     check_forward(msda, 3, inp, "f32", "3d f32 D=128")
 
 
+@pytest.mark.parametrize("nd,shape", [(2, (1, (1 << 23) - 1)), (3, ((1 << 23) - 1, 1, 2))],
+                         ids=["2d-W=2^23-1", "3d-Z=2^23-1"])
+def test_maximum_extents(msda, nd, shape):
+    """The largest extent the ABI accepts along one axis, 2^23 - 1 (2D: an 8.4 M-pixel row;
+    3D: as many slices): fp32 locations then resolve about half a pixel, and the cell is
+    still decided from the exact coordinate loc * extent - 0.5 on both sides.  Row indices
+    reach 2^23 and more, and the samples spread over the whole long axis."""
+    inp = workloads.random_problem(nd, [shape], B=1, Nq=48, M=1, D=4, P=4, seed=8,
+                                   margin=0.0)
+    check_forward(msda, nd, inp, "f32", f"max extent {shape} fwd")
+    check_backward(msda, nd, inp, "f32", f"max extent {shape} bwd")
+
+
 # ------------------------------------------------------------------ edge cases
 
 
