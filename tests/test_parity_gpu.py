@@ -152,6 +152,17 @@ def test_maximum_extents(msda, nd, shape):
     check_backward(msda, nd, inp, "f32", f"max extent {shape} bwd")
 
 
+def test_value_tensor_beyond_2gb(msda):
+    """A value tensor past 2^31 bytes (one 11600 x 11600 level, 16-byte rows: 2.15 GB) with
+    samples spread over all of it, so that about half of the corner rows sit beyond byte
+    offset 2^31: the 64-bit address arithmetic of the forward and backward."""
+    inp = workloads.random_problem(2, [(11600, 11600)], B=1, Nq=48, M=1, D=4, P=4, seed=9,
+                                   margin=0.0)
+    assert inp["value"].nbytes > 2 ** 31
+    check_forward(msda, 2, inp, "f32", "2.15 GB value fwd")
+    check_backward(msda, 2, inp, "f32", "2.15 GB value bwd")
+
+
 # ------------------------------------------------------------------ edge cases
 
 
