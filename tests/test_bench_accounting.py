@@ -1,0 +1,83 @@
+"""Host-side accounting of bench.py (no GPU): the algorithmic bytes behind the roofline
+fraction and the lookup of recorded DRAM traffic.
+
+The roofline's numerator counts each distinct value row that an in-level corner touches
+once ("unique value bytes").  bench.unique_value_rows computes it with vectorised numpy;
+here it is recounted by brute force, one sample and one corner at a time, on small drawn
+problems in 2D and 3D with samples straddling and leaving the levels.
+"""
+import math
+import os
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads  # noqa: E402
+
+
+def _brute_unique_rows(inp):
+    loc = inp["sampling_locations"].astype(np.float64)
+    B, Nq, M, L, P, nd = loc.shape
+    rows = set()
+    for b in range(B):
+        for q in range(Nq):
+            for m in range(M):
+                for l in range(L):
+                    ext = [int(e) for e in inp["spatial_shapes"][l][::-1]]   # (W, H[, Z])
+                    start = int(inp["level_start_index"][l])
+                    for p in range(P):
+                        pix = [loc[b, q, m, l, p, k] * ext[k] - 0.5 for k in range(nd)]
+                        if not all(math.isfinite(x) and -1 < x < e for x, e in zip(pix, ext)):
+                            continue
+                        base = [math.floor(x) for x in pix]
+                        for c in range(2 ** nd):
+                            idx = [base[k] + ((c >> k) & 1) for k in range(nd)]
+                            if not all(0 <= i < e for i, e in zip(idx, ext)):
+                                continue
+                            flat = idx[0] + ext[0] * idx[1]
+                            if nd == 3:
+                                flat += ext[0] * ext[1] * idx[2]
+                            rows.add((b, start + flat, m))
+    return len(rows)
+
+
+@pytest.mark.parametrize("nd,shapes", [(2, [(7, 9), (3, 4)]), (3, [(3, 4, 5), (2, 2, 3)])])
+def test_unique_value_rows_matches_brute_force(nd, shapes):
+    inp = workloads.random_problem(nd, shapes, B=2, Nq=23, M=3, D=8, P=3, seed=31)
+    w = workloads.Workload("t", nd, 2, tuple(tuple(s) for s in shapes), 23, 3, 8, 3, "f32", 31)
+    assert bench.unique_value_rows(w, inp) == _brute_unique_rows(inp)
+
+
+def test_algorithmic_bytes_of_the_encoder_forward():
+    """The encoder-shaped forward: locations, weights and output by size, and the unique
+    value bytes never above the whole value tensor."""
+    w = workloads.WORKLOADS["encoder2d"]
+    inp = workloads.make_inputs(w)
+    ab = bench.algorithmic_bytes(w, inp)
+    parts = ab["parts"]
+    samples = w.B * w.Nq * w.M * w.L * w.P
+    assert parts["locations"] == samples * 2 * 4 and parts["weights"] == samples * 4
+    assert parts["out"] == w.B * w.Nq * w.M * w.D * 4
+    assert 0 < parts["unique_value"] <= parts["whole_value_tensor"]
+    assert ab["total"] == sum(v for k, v in parts.items() if k != "whole_value_tensor")
+
+
+def test_recorded_traffic_is_keyed_by_workload_mode_and_source_hash(tmp_path, monkeypatch):
+    h = bench.kernel_source_hash("forward")
+    (tmp_path / "a.md").write_text(f"bench_workload: encoder2d\nkernel_source_sha256: {h}\n"
+                                   "dram_bytes_per_launch: 123\n")
+    (tmp_path / "b.md").write_text(f"bench_workload: encoder2d+order\nkernel_source_sha256: {h}\n"
+                                   "dram_bytes_per_launch: 456\n")
+    (tmp_path / "c.md").write_text("bench_workload: decoder2d\nkernel_source_sha256: "
+                                   + "0" * 64 + "\ndram_bytes_per_launch: 789\n")
+    monkeypatch.setattr(bench, "PROFILE_DIR", str(tmp_path))
+    assert bench.recorded_traffic("encoder2d") == 123
+    assert bench.recorded_traffic("encoder2d", "+order") == 456
+    assert bench.recorded_traffic("decoder2d") is None      # taken on other sources
+    assert bench.recorded_traffic("volume3d") is None       # no summary
