@@ -73,7 +73,9 @@ typedef struct CUstream_st *msda_stream_t;
 typedef enum {
     MSDA_OK = 0,
     MSDA_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent shapes, misalignment */
-    MSDA_ERR_UNSUPPORTED = 2, /* valid but outside the compiled set (D, L, P, dtype)      */
+    MSDA_ERR_UNSUPPORTED = 2, /* valid but outside what the library handles: D or dtype,
+                                 L / P above their maxima, extents of 2^23 or more, and
+                                 the fixed-scratch order's size limits                  */
     MSDA_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed                      */
     MSDA_ERR_INTERNAL = 4
 } msda_status;
