@@ -264,4 +264,18 @@ __device__ __forceinline__ Taps<NC> shfl_taps(const Taps<NC> &t, int src, int wi
     return r;
 }
 
+// 2D taps with the four corner-validity bits carried under the row index: five shuffles
+// instead of six.  The row of corner 0 lies in [-(W + 1), N_in), so it needs N_in < 2^27
+// (and W < 2^23, which the ABI guarantees); the caller checks p.pack_taps.
+__device__ __forceinline__ Taps<4> shfl_taps_packed(const Taps<4> &t, int src, int width) {
+    Taps<4> r;
+    const int v = __shfl_sync(kFull, static_cast<int>((static_cast<unsigned>(t.row) << 4) | t.ok),
+                              src, width);
+    r.row = v >> 4;
+    r.ok = static_cast<unsigned>(v) & 15u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) r.w[c] = __shfl_sync(kFull, t.w[c], src, width);
+    return r;
+}
+
 }  // namespace msda

@@ -253,7 +253,7 @@ template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 1, MI
 // l * P + p); its lane `sub` computes the taps of SPL of them.  The corner rows of the
 // next AHEAD samples are loaded before the current sample is summed.
 template <int DT, int G, int VB, int NDIM, int LL, int PP, int SPLIT, int AHEAD, int MINB,
-          bool FUSED>
+          bool FUSED, bool PACK = false>
 __global__ void __launch_bounds__(kFwdBlock, MINB)
 fwd_tiled(const __grid_constant__ Params p) {
     constexpr int N = VB / Vec<DT>::ESIZE;  // channels per lane
@@ -348,7 +348,10 @@ fwd_tiled(const __grid_constant__ Params p) {
     Slice<VB> u[DEPTH][NC];
     // taps of sample s from its owner lane, and its in-level corner rows
     auto fetch = [&](int s, int slot) {
-        tq[slot] = shfl_taps(tp[s % SPL], s / SPL, G);
+        if constexpr (PACK)
+            tq[slot] = shfl_taps_packed(tp[s % SPL], s / SPL, G);
+        else
+            tq[slot] = shfl_taps(tp[s % SPL], s / SPL, G);
         const int l = (s0 + s) / PP;  // a constant when SPLIT == 1
         const char *c0 = vb + static_cast<long long>(tq[slot].row) * p.rb32;
 #pragma unroll
@@ -410,12 +413,20 @@ cudaError_t launch_tiled(const Params &p, cudaStream_t s) {
     const long long threads = p.n_items * G * SPLIT;
     const long long blocks = (threads + kFwdBlock - 1) / kFwdBlock;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (p.ref)
+    if (p.ref) {
         fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, true>
             <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
-    else
+    } else if constexpr (NDIM == 2 && DT == kF32) {
+        if (p.pack_taps)
+            fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, false, true>
+                <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
+        else
+            fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, false>
+                <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
+    } else {
         fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, false>
             <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
+    }
     return cudaGetLastError();
 }
 

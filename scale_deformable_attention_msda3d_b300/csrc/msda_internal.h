@@ -37,6 +37,7 @@ struct Params {
     int M, D, L, P;
     long long row_bytes;        // M * D * sizeof(value dtype): stride between value rows
     int rb32;                   // row_bytes as a 32-bit int (validated to fit)
+    int pack_taps;              // N_in < 2^27: 2D taps may carry the validity bits in the row
     // level geometry (entries >= L unused)
     int W[kMaxLevels], H[kMaxLevels], Z[kMaxLevels], start[kMaxLevels];
     float fW[kMaxLevels], fH[kMaxLevels], fZ[kMaxLevels];
