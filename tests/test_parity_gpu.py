@@ -233,6 +233,75 @@ def test_non_default_stream(msda):
     check(host(out), oracle.run_inputs(2, inp), "f32", "side stream")
 
 
+def test_cuda_graph_capture_and_replay(msda):
+    """The calls enqueue plain kernel launches on the given stream and allocate nothing, so
+    a CUDA graph can capture them: replaying a captured forward + backward on new inputs
+    (copied into the captured buffers) matches the oracle on those inputs."""
+    torch = pytest.importorskip("torch")
+    first = workloads.random_problem(3, SHAPES3, B=1, Nq=90, M=4, D=32, P=4, seed=21)
+    second = workloads.random_problem(3, SHAPES3, B=1, Nq=90, M=4, D=32, P=4, seed=22)
+    dev = device_inputs(first, "f32")
+    out = torch.empty((1, 90, 4 * 32), dtype=torch.float32, device=dev["value"].device)
+    gv = torch.empty_like(dev["value"])
+    gl = torch.empty_like(dev["sampling_locations"])
+    ga = torch.empty_like(dev["attention_weights"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    args = (dev["value"], first["spatial_shapes"], first["level_start_index"],
+            dev["sampling_locations"], dev["attention_weights"])
+    with torch.cuda.stream(s):                       # warm-up outside the capture
+        msda.msda3d_forward(*args, out=out, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        msda.msda3d_forward(*args, out=out, stream=s)
+        msda.msda3d_backward(*args, dev["grad_out"], grad_value=gv, grad_sampling_locations=gl,
+                             grad_attention_weights=ga, stream=s)
+        g.capture_end()
+    new = device_inputs(second, "f32")
+    for k in ("value", "sampling_locations", "attention_weights", "grad_out"):
+        dev[k].copy_(new[k])
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    check(host(out), oracle.run_inputs(3, second), "f32", "graph replay forward")
+    rgv, rgl, rga = oracle.run_inputs(3, second, backward_pass=True)
+    check(host(gv), rgv, "f32", "graph replay grad_value", grad_value_magnitude(3, second))
+    check(host(gl), rgl, "f32", "graph replay grad_loc")
+    check(host(ga), rga, "f32", "graph replay grad_attn")
+
+
+def test_concurrent_streams(msda):
+    """Independent calls on four streams at once (different problems, 2D and 3D, both
+    dtypes) each match the oracle: the calls share no state on the device."""
+    torch = pytest.importorskip("torch")
+    cases = [(2, "f32", 31), (3, "bf16", 32), (2, "bf16", 33), (3, "f32", 34)]
+    streams = [torch.cuda.Stream() for _ in cases]
+    runs = []
+    for (nd, dtype, seed), st in zip(cases, streams):
+        inp = workloads.random_problem(nd, SHAPES2 if nd == 2 else SHAPES3, B=2, Nq=300, M=8,
+                                       D=32, P=4, dtype=dtype, seed=seed)
+        dev = device_inputs(inp, dtype)
+        st.wait_stream(torch.cuda.current_stream())
+        fwd = msda.msda2d_forward if nd == 2 else msda.msda3d_forward
+        bwd = msda.msda2d_backward if nd == 2 else msda.msda3d_backward
+        a = (dev["value"], inp["spatial_shapes"], inp["level_start_index"],
+             dev["sampling_locations"], dev["attention_weights"])
+        with torch.cuda.stream(st):
+            out = fwd(*a, stream=st)
+            grads = bwd(*a, dev["grad_out"], stream=st)
+        runs.append((nd, dtype, inp, out, grads))
+    torch.cuda.synchronize()
+    for nd, dtype, inp, out, (gv, gl, ga) in runs:
+        check(host(out), oracle.run_inputs(nd, inp), dtype, f"stream fwd {nd}d {dtype}")
+        rgv, rgl, rga = oracle.run_inputs(nd, inp, backward_pass=True)
+        check(host(gv), rgv, "f32" if dtype == "f32" else "bf16", f"stream grad_value {nd}d",
+              grad_value_magnitude(nd, inp))
+        check(host(gl), rgl, dtype, f"stream grad_loc {nd}d {dtype}")
+        check(host(ga), rga, dtype, f"stream grad_attn {nd}d {dtype}")
+
+
 def test_autograd_wrapper_matches_backward_call(msda):
     torch = pytest.importorskip("torch")
     inp = workloads.random_problem(2, SHAPES2, B=1, Nq=40, M=2, D=16, P=4, seed=16)
