@@ -81,3 +81,35 @@ def test_recorded_traffic_is_keyed_by_workload_mode_and_source_hash(tmp_path, mo
     assert bench.recorded_traffic("encoder2d", "+order") == 456
     assert bench.recorded_traffic("decoder2d") is None      # taken on other sources
     assert bench.recorded_traffic("volume3d") is None       # no summary
+
+
+def _run_bench(args, env_extra=None):
+    import json
+    import subprocess
+    env = dict(os.environ, **(env_extra or {}))
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    return [json.loads(l) for l in lines]
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the CPU oracle, no GPU) prints one JSON line with the
+    contract's keys, on the same metric and workload keys as the GPU arm."""
+    (line,) = _run_bench(["--impl", "reference", "--workload", "tiny2d", "--steps", "3",
+                          "--warmup", "3"])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "impl", "cpu_baseline", "e2e", "gpu_launches"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["steps"] == 3 and line["gpu_launches"] == 0
+    assert line["config"] == bench.workload_config(workloads.WORKLOADS["tiny2d"])
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["cores"] == 1
+
+
+def test_reference_arm_other_ranks_stay_silent():
+    """Under torchrun only rank 0 runs the reference arm; another rank prints nothing."""
+    assert _run_bench(["--impl", "reference", "--workload", "tiny2d", "--steps", "3",
+                       "--warmup", "3"], {"RANK": "1", "WORLD_SIZE": "2"}) == []
