@@ -143,7 +143,8 @@ def test_drawn_fused_problems_forward_and_backward(msda, problem):
     a = oracle.softmax_weights(f["attention_logits"])
     mag_v, _, _ = oracle.backward(*args, loc, a, np.abs(g))
     _, gl, _ = oracle.backward(*args, loc, a, g)
-    check(host(gv), rgv, "f32" if dtype == "f32" else "bf16", "drawn fused grad_value", mag_v)
-    check(host(goff), rgoff, dtype, "drawn fused grad_offsets")
-    check(host(gz), rgz, dtype, "drawn fused grad_logits")
-    check(host(gref), rgref, dtype, "drawn fused grad_ref", np.abs(gl).sum(axis=(2, 4)))
+    # the gradients are fp32 results, whatever the value dtype
+    check(host(gv), rgv, "f32", "drawn fused grad_value", mag_v)
+    check(host(goff), rgoff, "f32", "drawn fused grad_offsets")
+    check(host(gz), rgz, "f32", "drawn fused grad_logits")
+    check(host(gref), rgref, "f32", "drawn fused grad_ref", np.abs(gl).sum(axis=(2, 4)))

@@ -55,7 +55,10 @@ def test_pruned_forward_matches_oracle_and_bound(msda, nd, shapes, dtype, D, P):
         got = _pruned(msda, nd, d, tau)
         check(got, oracle.forward_pruned(*a, tau), dtype, f"pruned tau={tau}")
         bound = oracle.pruning_bound(*a, tau)
-        slack = 2e-2 if dtype == "bf16" else 1e-5 * max(1.0, float(np.abs(exact).max()))
+        # rounding of the GPU result: the fp32 bound, plus half a bf16 ulp when stored in bf16
+        slack = 1e-5 * max(1.0, float(np.abs(exact).max()))
+        if dtype == "bf16":
+            slack = slack + 2.0 ** -8 * np.abs(got)
         assert np.all(np.abs(got - oracle.forward(*a)) <= bound + slack)
     big = 2 * float(np.abs(inp["attention_weights"]).max())
     assert np.all(_pruned(msda, nd, d, big) == 0.0)
