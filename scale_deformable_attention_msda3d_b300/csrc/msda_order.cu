@@ -129,11 +129,13 @@ cudaError_t launch_query_order(int ndim, const Params &p, int *order, int *hist,
                                cudaStream_t s) {
     const long long n = p.B * p.Nq;
     if (n == 0) return cudaSuccess;
+    // every grid size is checked before the first enqueue: a rejected call leaves nothing
+    // on the stream
+    const long long warps_blocks = (n * 32 + 255) / 256;
+    if (warps_blocks > 0x7fffffffLL || p.B > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
     cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(int) * p.B * kOrderBuckets, s);
     if (e != cudaSuccess) return e;
-    const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
-    const long long warps_blocks = (n * 32 + 255) / 256;
-    if (warps_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int per_query = p.M * p.L * p.P;
     if (ndim == 2)
         order_keys<2><<<static_cast<unsigned>(warps_blocks), 256, 0, s>>>(p.loc, n, per_query,

@@ -275,3 +275,73 @@ def test_extents_of_2_23_or_more_are_unsupported(lib):
         d2 = msda.make_dims(1, big + 1, 4, 1, 4, 1, 4, msda.MSDA_F32)
         st = msda.forward_raw(nd, d2, FAKE, sh2, np.array([0]), FAKE, FAKE, FAKE, 0)
         assert st == msda.MSDA_ERR_UNSUPPORTED and "2^23" in msda.msda_last_error()
+
+
+# ------------------------------------------------------------------ MSDA_ERR_CUDA
+
+# Runs in a child process that sees no CUDA device (CUDA_VISIBLE_DEVICES=""): every call
+# below passes validation, so its first CUDA runtime call (a kernel launch, a memset or
+# cudaGetDevice) fails and the library must return MSDA_ERR_CUDA with the runtime's
+# message.  The pointers are aligned integers that nothing dereferences: without a device
+# nothing is enqueued.
+_NO_DEVICE_SCRIPT = r"""
+import json, sys
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+import scale_deformable_attention_msda3d_b300 as msda
+msda.load()
+F = 0x10000
+SH = {2: np.array([[4, 6], [2, 3]]), 3: np.array([[2, 4, 6], [1, 2, 3]])}
+LS = {2: np.array([0, 24]), 3: np.array([0, 48])}
+NIN = {2: 30, 3: 54}
+res = {}
+for nd in (2, 3):
+    for dt in (msda.MSDA_F32, msda.MSDA_BF16):
+        d = msda.make_dims(2, NIN[nd], 5, 2, 8, 2, 4, dt)
+        sh, ls = SH[nd], LS[nd]
+        calls = {
+            "forward": lambda: msda.forward_raw(nd, d, F, sh, ls, F, F, F, 0),
+            "forward_fused": lambda: msda.forward_fused_raw(nd, d, F, sh, ls, F, F, F, F, 0),
+            "forward_pruned": lambda: msda.forward_pruned_raw(nd, d, F, sh, ls, F, F, 0.01, F, 0),
+            "forward_ordered": lambda: msda.forward_ordered_raw(nd, d, F, sh, ls, F, F, F, F, 0),
+            "backward": lambda: msda.backward_raw(nd, d, F, sh, ls, F, F, F, F, F, F, 0),
+            "backward_fused": lambda: msda.backward_fused_raw(nd, d, F, sh, ls, F, F, F, F, F, F,
+                                                              F, F, 0),
+            "query_order": lambda: msda.query_order_raw(nd, d, F, F, F, 1 << 24, 0),
+            "query_order_static": lambda: msda.query_order_static_raw(nd, d, F, F, 0),
+        }
+        for name, fn in calls.items():
+            st = int(fn())
+            res[f"{name}/{nd}d/{dt}"] = [st, msda.msda_last_error()]
+print(json.dumps(res))
+"""
+
+
+def test_cuda_errors_map_to_msda_err_cuda_without_a_device():
+    """Every public compute call returns MSDA_ERR_CUDA, with the runtime's error in
+    msda_last_error(), when its first CUDA runtime call fails (here: no visible device)."""
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", _NO_DEVICE_SCRIPT, ROOT], env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert len(res) == 2 * 2 * 8
+    for key, (st, msg) in res.items():
+        assert st == msda.MSDA_ERR_CUDA, (key, st, msg)
+        # "<what>: <cudaError name> (<description>)"
+        assert re.search(r": cudaError\w+ \(", msg), (key, msg)
+
+
+def test_query_order_grid_too_large_is_a_cuda_error_with_nothing_enqueued(lib):
+    """B * Nq beyond what one grid of one warp per query can hold: the launch layer
+    returns cudaErrorInvalidConfiguration before its first enqueue (the histogram clear
+    included), so the call fails with MSDA_ERR_CUDA without touching the device."""
+    d = dims(B=9, Nq=2 ** 31 - 1)                     # 1.9e10 queries > 2^34
+    st, need = msda.query_order_workspace_raw(2, d)
+    assert st == msda.MSDA_OK
+    st = msda.query_order_raw(2, d, FAKE, FAKE, FAKE, need, 0)
+    assert st == msda.MSDA_ERR_CUDA, msda.msda_last_error()
+    assert "cudaErrorInvalidConfiguration" in msda.msda_last_error()
