@@ -33,7 +33,7 @@ def compile_source(src: str, out_path: str) -> str:
     """Compile an oracle source file with gcc (IEEE double, no FMA contraction)."""
     tmp = out_path + f".tmp{os.getpid()}"
     subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-                    "-shared", "-fPIC", "-o", tmp, src, "-lm"], check=True)
+                    "-fopenmp", "-shared", "-fPIC", "-o", tmp, src, "-lm"], check=True)
     os.replace(tmp, out_path)
     return out_path
 
@@ -63,6 +63,11 @@ def _bind(path: str):
     for name in ("oracle_msda2d_backward", "oracle_msda3d_backward"):
         getattr(lib, name).argtypes = bwd_args
         getattr(lib, name).restype = ctypes.c_int
+    if hasattr(lib, "oracle_msda2d_forward_threads"):
+        for name in ("oracle_msda2d_forward_threads", "oracle_msda3d_forward_threads"):
+            getattr(lib, name).argtypes = fwd_args + [ctypes.c_int]
+            getattr(lib, name).restype = ctypes.c_int
+        lib.oracle_default_threads.restype = ctypes.c_int
     return lib
 
 
@@ -95,17 +100,29 @@ def _dims(value: np.ndarray, loc: np.ndarray, shapes: np.ndarray, nd: int):
     return B, Nin, Nq, M, D, L, P
 
 
+def default_threads() -> int:
+    """Threads the oracle's multi-core forward uses by default (OpenMP's count)."""
+    return int(_load().oracle_default_threads())
+
+
 def forward(nd: int, value, spatial_shapes, level_start_index, sampling_locations,
-            attention_weights, lib=None) -> np.ndarray:
-    """out[B, Nq, M*D] in float64.  ``lib`` selects another build of the oracle."""
+            attention_weights, lib=None, threads: int = 1) -> np.ndarray:
+    """out[B, Nq, M*D] in float64.  ``lib`` selects another build of the oracle.
+    ``threads`` != 1 runs the same serial forward on blocks of queries over that many
+    host threads (0: OpenMP's default); every output is computed identically."""
     v, loc, a = _d(value), _d(sampling_locations), _d(attention_weights)
     sh, ls = _i(spatial_shapes), _i(level_start_index)
     B, Nin, Nq, M, D, L, P = _dims(v, loc, sh, nd)
     out = np.zeros((B, Nq, M * D), dtype=np.float64)
     lib = lib or _load()
-    fn = lib.oracle_msda2d_forward if nd == 2 else lib.oracle_msda3d_forward
-    rc = fn(B, Nin, Nq, M, D, L, P, _ptr(sh, _LP), _ptr(ls, _LP), _ptr(v, _DP),
+    args = (B, Nin, Nq, M, D, L, P, _ptr(sh, _LP), _ptr(ls, _LP), _ptr(v, _DP),
             _ptr(loc, _DP), _ptr(a, _DP), _ptr(out, _DP))
+    if threads != 1:
+        fn = lib.oracle_msda2d_forward_threads if nd == 2 else lib.oracle_msda3d_forward_threads
+        rc = fn(*args, int(threads))
+    else:
+        fn = lib.oracle_msda2d_forward if nd == 2 else lib.oracle_msda3d_forward
+        rc = fn(*args)
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return out
@@ -180,12 +197,12 @@ def softmax_weights(attention_logits) -> np.ndarray:
 
 
 def forward_fused(nd: int, value, spatial_shapes, level_start_index, reference_points,
-                  sampling_offsets, attention_logits, lib=None) -> np.ndarray:
+                  sampling_offsets, attention_logits, lib=None, threads: int = 1) -> np.ndarray:
     """The core fed by the module's prologue: locations from reference points and offsets
     (fp32, as above), weights from a double-precision softmax of the logits."""
     loc = fused_locations(spatial_shapes, reference_points, sampling_offsets)
     return forward(nd, value, spatial_shapes, level_start_index, loc,
-                   softmax_weights(attention_logits), lib=lib)
+                   softmax_weights(attention_logits), lib=lib, threads=threads)
 
 
 def backward_fused(nd: int, value, spatial_shapes, level_start_index, reference_points,
@@ -216,7 +233,7 @@ def backward_fused(nd: int, value, spatial_shapes, level_start_index, reference_
 
 
 def forward_pruned(nd: int, value, spatial_shapes, level_start_index, sampling_locations,
-                   attention_weights, threshold: float, lib=None) -> np.ndarray:
+                   attention_weights, threshold: float, lib=None, threads: int = 1) -> np.ndarray:
     """The core with probability-aware pruning of sampling points ("DEFA: Efficient
     Deformable Attention Acceleration via Pruning-Assisted Grid-Sampling and Multi-Scale
     Parallel Processing", abstract): a sample whose weight has |A| < threshold is dropped
@@ -226,7 +243,7 @@ def forward_pruned(nd: int, value, spatial_shapes, level_start_index, sampling_l
     a = np.asarray(attention_weights, dtype=np.float64)
     a = np.where(np.abs(a) < threshold, 0.0, a)
     return forward(nd, value, spatial_shapes, level_start_index, sampling_locations, a,
-                   lib=lib)
+                   lib=lib, threads=threads)
 
 
 def pruning_bound(nd: int, value, spatial_shapes, level_start_index, sampling_locations,

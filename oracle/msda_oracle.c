@@ -34,11 +34,15 @@
  *   gradient there is that cell's (right-hand) derivative.
  *
  * Every floating-point input is passed as double (fp32 and bf16 values widen exactly).
- * Build: gcc -O2 -std=c11 -ffp-contract=off -shared -fPIC.
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -shared -fPIC (OpenMP only splits
+ * the forward's queries across threads, for timing on all host cores; see the end).
  */
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* ------------------------------------------------------------------------- */
 /* 2D                                                                        */
@@ -288,4 +292,74 @@ int oracle_msda3d_backward(int64_t B, int64_t Nin, int64_t Nq, int64_t M, int64_
         }
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Forward over all host cores (for timing the oracle as a CPU baseline)     */
+/* ------------------------------------------------------------------------- */
+
+/* Every output row (b, q) of the forward depends only on its own locations and weights,
+ * so the forward over all queries equals the forward over any split of the queries.
+ * These entry points cut each batch's queries into blocks of OR_BLOCK and hand the
+ * blocks to OpenMP threads; each block runs the serial forward above, unchanged, on its
+ * slice (B = 1, Nq = block size), so every output is computed by the same arithmetic in
+ * the same order as in the serial call.  nthreads <= 0 uses OpenMP's default. */
+#define OR_BLOCK 64
+
+typedef int (*oracle_fwd_fn)(int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t,
+                             const int64_t *, const int64_t *, const double *, const double *,
+                             const double *, double *);
+
+static int forward_blocks(oracle_fwd_fn fn, int nd, int64_t B, int64_t Nin, int64_t Nq,
+                          int64_t M, int64_t D, int64_t L, int64_t P, const int64_t *shapes,
+                          const int64_t *level_start, const double *value, const double *loc,
+                          const double *attn, double *out, int nthreads)
+{
+    if (check_common(B, Nin, Nq, M, D, L, P)) return 1;
+    const int64_t per_b = (Nq + OR_BLOCK - 1) / OR_BLOCK;
+    const int64_t total = B * per_b;
+    const int64_t S = M * L * P; /* samples per query */
+    int rc = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : rc) num_threads(nthreads > 0 ? nthreads : omp_get_max_threads())
+#endif
+    for (int64_t t = 0; t < total; ++t) {
+        const int64_t b = t / per_b;
+        const int64_t q0 = (t % per_b) * OR_BLOCK;
+        const int64_t nq = (Nq - q0) < OR_BLOCK ? (Nq - q0) : OR_BLOCK;
+        const int64_t first = b * Nq + q0; /* first (b, q) row of the block */
+        rc |= fn(1, Nin, nq, M, D, L, P, shapes, level_start, value + b * Nin * M * D,
+                 loc + first * S * nd, attn + first * S, out + first * M * D);
+    }
+    return rc;
+}
+
+int oracle_msda2d_forward_threads(int64_t B, int64_t Nin, int64_t Nq, int64_t M, int64_t D,
+                                  int64_t L, int64_t P, const int64_t *shapes,
+                                  const int64_t *level_start, const double *value,
+                                  const double *loc, const double *attn, double *out,
+                                  int nthreads)
+{
+    return forward_blocks(oracle_msda2d_forward, 2, B, Nin, Nq, M, D, L, P, shapes,
+                          level_start, value, loc, attn, out, nthreads);
+}
+
+int oracle_msda3d_forward_threads(int64_t B, int64_t Nin, int64_t Nq, int64_t M, int64_t D,
+                                  int64_t L, int64_t P, const int64_t *shapes,
+                                  const int64_t *level_start, const double *value,
+                                  const double *loc, const double *attn, double *out,
+                                  int nthreads)
+{
+    return forward_blocks(oracle_msda3d_forward, 3, B, Nin, Nq, M, D, L, P, shapes,
+                          level_start, value, loc, attn, out, nthreads);
+}
+
+/* Threads an OpenMP parallel region of this build gets by default (1 without OpenMP). */
+int oracle_default_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
 }

@@ -263,3 +263,19 @@ def test_fused_backward_logit_gradients_sum_to_zero(oracle_mod):
         c["sampling_offsets"], c["attention_logits"], c["grad_out"])
     s = g_logit.reshape(g_logit.shape[:3] + (-1,)).sum(-1)
     assert np.allclose(s, 0.0, atol=1e-12)
+
+
+@pytest.mark.parametrize("nd", [2, 3])
+def test_multicore_forward_equals_the_serial_forward(oracle_mod, nd):
+    """The oracle's all-core forward (used to time it on every host core) cuts the queries
+    into blocks and runs the serial forward on each: every output must be bit-identical to
+    the serial call, with batch > 1 and a query count that leaves a ragged last block."""
+    import workloads
+    shapes = [(9, 11), (5, 6)] if nd == 2 else [(4, 5, 6), (2, 3, 3)]
+    inp = workloads.random_problem(nd, shapes, B=3, Nq=150, M=3, D=8, P=3, seed=71,
+                                   backward=False)
+    args = (nd, inp["value"], inp["spatial_shapes"], inp["level_start_index"],
+            inp["sampling_locations"], inp["attention_weights"])
+    serial = oracle_mod.forward(*args)
+    for t in (2, 5, 0):
+        assert np.array_equal(oracle_mod.forward(*args, threads=t), serial), t
