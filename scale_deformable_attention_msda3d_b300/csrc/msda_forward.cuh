@@ -19,12 +19,14 @@
 // Two kernels:
 // * fwd_tiled (the compiled (L, P) pairs): the locations and weights of an item are read
 //   once with vector loads, spread over the lanes of its group; each lane works out the
-//   cell, corner validity and weights of its own samples, and the group then walks the
-//   samples in order, taking each sample's corner data from its owner by warp shuffle and
-//   loading the corner rows of the next AHEAD samples before summing the current one.
-//   Optionally the item's samples are split over SPLIT lane groups whose partial sums are
-//   added by shuffles at the end (fewer taps per lane for narrow rows, more loads in flight
-//   when there are few items).  3D uses 32-byte (256-bit) loads per lane.
+//   cell, corner validity and fractions of its own samples and leaves them in shared
+//   memory (one 16-byte record per sample), and the group then walks the samples in
+//   order, reading each sample's record, loading the corner rows of the next AHEAD samples
+//   (in-level corners only, without zeroing the others) before summing the current one
+//   under the same per-corner predicates.  Optionally the item's samples are split over
+//   SPLIT lane groups whose partial sums are added by shuffles at the end (fewer taps per
+//   lane for narrow rows, more loads in flight when there are few items).  3D uses
+//   32-byte (256-bit) loads per lane.
 // * fwd{2,3}d_generic (any L, P): every lane of the group computes every sample itself.
 #pragma once
 
@@ -235,25 +237,76 @@ __device__ __forceinline__ uint4 pack16(const float2 *acc) {
 // Launch shape of the compiled path for one (ndim, dtype): bytes per lane and row (VB),
 // samples whose corner rows are in flight ahead of the one being summed (AHEAD), and the
 // minimum resident blocks of kFwdBlock threads per SM that caps registers (MINB).  Tuned
-// on B300 with the encoder (fp32 2D), decoder (bf16 2D) and volume (bf16 3D) workloads:
-// the gather is bound by how many corner rows are in flight per SM, so occupancy is worth
-// more than depth; 3D's 8 corners per sample favour 256-bit loads.
+// on B300 with the encoder (fp32 2D), decoder (bf16 2D) and volume (bf16 3D) workloads.
+// 16-byte lanes keep one L1 wavefront per 128-byte row (256-bit lanes over 128-byte rows
+// cost about 1.5); 3D's 64-byte bf16 rows take 32-byte lanes (two lanes per row).
 // Blocks are kFwdBlock = 128 threads: finished work is replaced at a finer grain than with
-// 256 (items take uneven time, e.g. skipped out-of-level corners), worth 6% on the encoder
-// workload.
+// 256 (items take uneven time, e.g. skipped out-of-level corners).
+// PRED: out-of-level corners are skipped by predicating their loads and FMAs (no zeroed
+// registers); without it (the wide 3D slices, where the predicated form needs more
+// registers than the block budget) their slices are zeroed before the predicated load and
+// their weights set to zero, and every FMA runs.
 constexpr int kFwdBlock = 128;
 template <int NDIM, int DT> struct Shape;
-template <> struct Shape<2, kF32> { static constexpr int VB = 16, AHEAD = 1, MINB = 12; };
-template <> struct Shape<2, kBF16> { static constexpr int VB = 16, AHEAD = 1, MINB = 10; };
-template <> struct Shape<3, kF32> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; };
-template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; };
+template <> struct Shape<2, kF32> { static constexpr int VB = 16, AHEAD = 2, MINB = 12; static constexpr bool PRED = true; };
+template <> struct Shape<2, kBF16> { static constexpr int VB = 16, AHEAD = 1, MINB = 10; static constexpr bool PRED = false; };
+template <> struct Shape<3, kF32> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; static constexpr bool PRED = false; };
+template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; static constexpr bool PRED = false; };
+
+// Shared-memory slot of sample s of an item: one pad slot after every 8, so that the 8
+// lanes of a group writing their samples' records (two consecutive samples each) hit
+// distinct banks.
+__host__ __device__ constexpr int tap_slot(int s) { return s + (s >> 3); }
+
+// Corner data ("tap record") of one sample, as the lane that computed it leaves it in
+// shared memory for the other lanes of its group: rec.x = value row of corner 0 (int bits;
+// with PACK the validity bits sit under it), rec.y = attention weight a, rec.z / rec.w =
+// fractions fx / fy; 3D adds fz (and the validity bits when not packed) in a second array.
+// A reader forms the corner weights from (a, fx, fy[, fz]) with the same expressions as
+// make_taps, so its weights are bit-identical to the owner's.  Four words instead of the
+// four weights: one shared-memory wavefront less per warp step.
+template <int NC> struct TapView {
+    int row;
+    unsigned ok;
+    float w[NC];
+};
+
+__device__ __forceinline__ void tap_weights(float a, float fx, float fy, float (&w)[4]) {
+    const float ay0 = a * (1.f - fy), ay1 = a * fy;
+    w[0] = ay0 * (1.f - fx);
+    w[1] = ay0 * fx;
+    w[2] = ay1 * (1.f - fx);
+    w[3] = ay1 * fx;
+}
+__device__ __forceinline__ void tap_weights(float a, float fx, float fy, float fz, float (&w)[8]) {
+    const float wx[2] = {1.f - fx, fx};
+    const float wy[2] = {1.f - fy, fy};
+    const float wz[2] = {a * (1.f - fz), a * fz};
+#pragma unroll
+    for (int c = 0; c < 8; ++c) w[c] = (wz[c >> 2] * wy[(c >> 1) & 1]) * wx[c & 1];
+}
+
+// Slice load under a predicate, without zeroing: when `pred` is false the destination
+// holds an unspecified value and the caller must not read it (the matching FMAs are under
+// the same predicate).  The empty asm gives the compiler a value to start from that costs
+// no instruction; the load itself stays behind the branch.
+__device__ __forceinline__ void load_slice_if(bool pred, const char *p, Slice<16> &r) {
+    asm("" : "=r"(r.a.x), "=r"(r.a.y), "=r"(r.a.z), "=r"(r.a.w));
+    if (pred) r.a = ldg16(p);
+}
+__device__ __forceinline__ void load_slice_if(bool pred, const char *p, Slice<32> &r) {
+    asm("" : "=r"(r.a.x), "=r"(r.a.y), "=r"(r.a.z), "=r"(r.a.w), "=r"(r.b.x), "=r"(r.b.y),
+             "=r"(r.b.z), "=r"(r.b.w));
+    if (pred) ldg32(p, r.a, r.b);
+}
 
 // One item = (b, q, m); LANES = G * SPLIT lanes per item; lane = (item, sp, sub).
 // Subgroup sp handles samples [sp * SS, (sp + 1) * SS) of the item (sample index
-// l * P + p); its lane `sub` computes the taps of SPL of them.  The corner rows of the
-// next AHEAD samples are loaded before the current sample is summed.
+// l * P + p); its lane `sub` computes the taps of SPL of them and leaves their records in
+// shared memory.  The group then walks its samples: the corner rows of the next AHEAD
+// samples are loaded (in-level corners only) before the current sample is summed.
 template <int DT, int G, int VB, int NDIM, int LL, int PP, int SPLIT, int AHEAD, int MINB,
-          bool FUSED, bool PACK = false>
+          bool FUSED, bool PACK, bool PRED>
 __global__ void __launch_bounds__(kFwdBlock, MINB)
 fwd_tiled(const __grid_constant__ Params p) {
     constexpr int N = VB / Vec<DT>::ESIZE;  // channels per lane
@@ -269,23 +322,43 @@ fwd_tiled(const __grid_constant__ Params p) {
     constexpr int ALOC = cmin(cmin(falign(S * NDIM), falign(SS * NDIM)), falign(SPL * NDIM));
     constexpr int AATT = cmin(cmin(falign(S), falign(SS)), falign(SPL));
     constexpr int DEPTH = AHEAD + 1;
+    constexpr int IPB = kFwdBlock / LANES;            // items per block
+    constexpr int ISTR = tap_slot(S - 1) + 2;         // slots per item (+1 pad between items)
+    constexpr int OKB = NDIM == 2 ? 4 : 8;            // validity bits under a packed row
+
+    __shared__ float4 rec[IPB * ISTR];
+    __shared__ float rec_z[NDIM == 3 ? IPB * ISTR : 1];               // fz (3D)
+    __shared__ unsigned rec_ok[PACK ? 1 : IPB * ISTR];                // validity bits
 
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    // whole warps leave together: the shuffles below need every lane of the warp
+    // whole warps leave together: the exchange below needs every lane of the warp
     if ((t & ~31LL) / LANES >= p.n_items) return;
     long long pos = t / LANES;
     const bool active = pos < p.n_items;
     if (!active) pos = p.n_items - 1;  // tail lanes redo a real item and store nothing
-    const long long item = ordered_item(p, pos);
+    long long item;
+    int m;
+    long long b;
+    if (p.order == nullptr && p.n_items <= 0x7fffffffLL) {
+        // 32-bit index arithmetic (the launch checks the item count)
+        const unsigned it = static_cast<unsigned>(pos);
+        const unsigned bq = it / static_cast<unsigned>(p.M);
+        m = static_cast<int>(it - bq * static_cast<unsigned>(p.M));
+        b = bq / static_cast<unsigned>(p.Nq);
+        item = it;
+    } else {
+        item = ordered_item(p, pos);
+        m = static_cast<int>(item % p.M);
+        b = item / p.M / p.Nq;
+    }
     const int lane = threadIdx.x & 31;
     const int sub = lane & (G - 1);
     const int sp = SPLIT > 1 ? (lane / G) & (SPLIT - 1) : 0;
-    const int m = static_cast<int>(item % p.M);
-    const long long b = item / p.M / p.Nq;
+    const int ib = threadIdx.x / LANES;       // item within the block
     const int s0 = sp * SS;                  // first sample of this subgroup
     const int my0 = s0 + sub * SPL;          // first sample whose taps this lane computes
 
-    // 1. locations and weights of this lane's samples, then their taps
+    // 1. locations and weights of this lane's samples, then their tap records
     float lv[SPL * NDIM], av[SPL];
     const float *lsrc = p.loc + (item * S + my0) * NDIM;
     const float *asrc = p.attn + item * S + my0;
@@ -327,14 +400,21 @@ fwd_tiled(const __grid_constant__ Params p) {
                 lv[i * NDIM + k] = fused_location<NDIM>(p, bq, l, k, lv[i * NDIM + k]);
         }
     }
-    Taps<NC> tp[SPL];
 #pragma unroll
     for (int i = 0; i < SPL; ++i) {
-        // a lane past the end of the subgroup's samples computes a harmless copy of
-        // sample my0 clamped into range (never shuffled out)
-        const int j = cmin(my0 + i, s0 + SS - 1);
-        make_taps(p, j / PP, lv + i * NDIM, av[i], tp[i]);
+        if (!EVEN && sub * SPL + i >= SS) continue;   // past the subgroup's samples
+        const int j = my0 + i;
+        Taps<NC> tp;
+        float fr[NDIM];
+        make_taps(p, j / PP, lv + i * NDIM, av[i], tp, fr);
+        const int slot = ib * ISTR + tap_slot(j);
+        const int rbits = PACK ? static_cast<int>((static_cast<unsigned>(tp.row) << OKB) | tp.ok)
+                               : tp.row;
+        rec[slot] = make_float4(__int_as_float(rbits), av[i], fr[0], fr[1]);
+        if constexpr (NDIM == 3) rec_z[slot] = fr[2];
+        if constexpr (!PACK) rec_ok[slot] = tp.ok;
     }
+    __syncwarp();
 
     // 2. walk the subgroup's samples; corner rows are VB-byte slices per lane
     const long long rb = p.row_bytes;
@@ -344,24 +424,40 @@ fwd_tiled(const __grid_constant__ Params p) {
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) acc[i] = make_float2(0.f, 0.f);
 
-    Taps<NC> tq[DEPTH];
+    TapView<NC> tq[DEPTH];
     Slice<VB> u[DEPTH][NC];
-    // taps of sample s from its owner lane, and its in-level corner rows
+    // record of sample s0 + s, then its in-level corner rows
     auto fetch = [&](int s, int slot) {
-        if constexpr (PACK)
-            tq[slot] = shfl_taps_packed(tp[s % SPL], s / SPL, G);
-        else
-            tq[slot] = shfl_taps(tp[s % SPL], s / SPL, G);
+        const int j = ib * ISTR + tap_slot(s0 + s);
+        const float4 r = rec[j];
+        if constexpr (PACK) {
+            const int v = __float_as_int(r.x);
+            tq[slot].row = v >> OKB;
+            tq[slot].ok = static_cast<unsigned>(v) & ((1u << OKB) - 1u);
+        } else {
+            tq[slot].row = __float_as_int(r.x);
+            tq[slot].ok = rec_ok[j];
+        }
+        if constexpr (NDIM == 2) tap_weights(r.y, r.z, r.w, tq[slot].w);
+        else tap_weights(r.y, r.z, r.w, rec_z[j], tq[slot].w);
+        if constexpr (!PRED) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c) tq[slot].w[c] = ((tq[slot].ok >> c) & 1u) ? tq[slot].w[c] : 0.f;
+        }
         const int l = (s0 + s) / PP;  // a constant when SPLIT == 1
         const char *c0 = vb + static_cast<long long>(tq[slot].row) * p.rb32;
+        const char *cy[2] = {c0, c0 + p.sy[l]};
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-            const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
-            long long off = dx ? rb : 0;
-            if (dy) off += p.sy[l];
-            if (dz) off += p.sz[l];
-            zero_slice(u[slot][c]);
-            if (tq[slot].ok & (1u << c)) load_slice(c0 + off, u[slot][c]);
+            const char *base = cy[(c >> 1) & 1];
+            if (c >> 2) base += p.sz[l];
+            const bool in = (tq[slot].ok >> c) & 1u;
+            if constexpr (PRED) {
+                load_slice_if(in, base + ((c & 1) ? rb : 0), u[slot][c]);
+            } else {
+                zero_slice(u[slot][c]);
+                if (in) load_slice(base + ((c & 1) ? rb : 0), u[slot][c]);
+            }
         }
     };
 #pragma unroll
@@ -372,7 +468,8 @@ fwd_tiled(const __grid_constant__ Params p) {
         if (s + AHEAD < SS) fetch(s + AHEAD, (s + AHEAD) % DEPTH);
         const int slot = s % DEPTH;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) fma_slice<DT, VB>(acc, tq[slot].w[c], u[slot][c]);
+        for (int c = 0; c < NC; ++c)
+            if (!PRED || ((tq[slot].ok >> c) & 1u)) fma_slice<DT, VB>(acc, tq[slot].w[c], u[slot][c]);
     }
 
     // 3. add the subgroups' partial sums, store the item's channels
@@ -413,19 +510,21 @@ cudaError_t launch_tiled(const Params &p, cudaStream_t s) {
     const long long threads = p.n_items * G * SPLIT;
     const long long blocks = (threads + kFwdBlock - 1) / kFwdBlock;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(blocks));
     if (p.ref) {
-        fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, true>
-            <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
-    } else if constexpr (NDIM == 2 && DT == kF32) {
         if (p.pack_taps)
-            fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, false, true>
-                <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
+            fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, true, true, SH::PRED>
+                <<<grid, kFwdBlock, 0, s>>>(p);
         else
-            fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, false>
-                <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
+            fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, true, false, SH::PRED>
+                <<<grid, kFwdBlock, 0, s>>>(p);
     } else {
-        fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, false>
-            <<<static_cast<unsigned>(blocks), kFwdBlock, 0, s>>>(p);
+        if (p.pack_taps)
+            fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, false, true, SH::PRED>
+                <<<grid, kFwdBlock, 0, s>>>(p);
+        else
+            fwd_tiled<DT, G, SH::VB, NDIM, LL, PP, SPLIT, SH::AHEAD, SH::MINB, false, false, SH::PRED>
+                <<<grid, kFwdBlock, 0, s>>>(p);
     }
     return cudaGetLastError();
 }

@@ -37,7 +37,8 @@ struct Params {
     int M, D, L, P;
     long long row_bytes;        // M * D * sizeof(value dtype): stride between value rows
     int rb32;                   // row_bytes as a 32-bit int (validated to fit)
-    int pack_taps;              // N_in < 2^27: 2D taps may carry the validity bits in the row
+    int pack_taps;              // forward tap records may carry the validity bits under the
+                                // row (N_in < 2^27 in 2D, < 2^22 in 3D)
     // level geometry (entries >= L unused)
     int W[kMaxLevels], H[kMaxLevels], Z[kMaxLevels], start[kMaxLevels];
     float fW[kMaxLevels], fH[kMaxLevels], fZ[kMaxLevels];
