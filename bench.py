@@ -45,7 +45,7 @@ METRIC = "sampled points/s (B·Nq·M·L·P per s) and achieved HBM GB/s vs ~8 TB
 UNIT = "samples/s"
 NOMINAL_HBM_GBS = 7700.0  # B300 HBM3e nominal bandwidth
 FALLBACK_HBM_GBS = 6400.0
-L2_BYTES = 126 * 2 ** 20
+L1_WAVEFRONT_BYTES = 128   # bytes one L1 data-pipe wavefront delivers; one per SM clock
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SRC_DIR = os.path.join(ROOT, "scale_deformable_attention_msda3d_b300", "csrc")
 
@@ -84,12 +84,14 @@ def kernel_source_hash(kind: str = "forward") -> str:
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str, mode: str = ""):
-    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if it was
-    taken on the current sources of that kernel family (else None).  A summary names its
-    bench workload, with "+order" / "+fused" / "+prune<t>" appended for those modes."""
+def recorded_counter(workload: str, mode: str = "", key: str = "dram_bytes_per_launch"):
+    """A per-launch counter of the dominant kernel (`key`: dram_bytes_per_launch or
+    l1_wavefronts_per_launch) from a committed ncu summary, if that summary was taken on
+    the current sources of the kernel family (else None).  A summary names its bench
+    workload, with "+order" / "+fused" / "+prune<t>" / "+order_once" appended for those
+    modes."""
     src = kernel_source_hash("backward" if workloads.WORKLOADS[workload].backward else "forward")
-    key = workload + mode
+    want = workload + mode
     if not os.path.isdir(PROFILE_DIR):
         return None
     for f in sorted(os.listdir(PROFILE_DIR)):
@@ -98,10 +100,51 @@ def recorded_traffic(workload: str, mode: str = ""):
         text = open(os.path.join(PROFILE_DIR, f)).read()
         m_w = re.search(r"^bench_workload:\s*(\S+)", text, re.M)
         m_h = re.search(r"^kernel_source_sha256:\s*([0-9a-f]{64})", text, re.M)
-        m_t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-        if m_w and m_h and m_t and m_w.group(1) == key and m_h.group(1) == src:
+        m_t = re.search(r"^" + re.escape(key) + r":\s*([0-9.eE+]+)", text, re.M)
+        if m_w and m_h and m_t and m_w.group(1) == want and m_h.group(1) == src:
             return float(m_t.group(1))
     return None
+
+
+def recorded_traffic(workload: str, mode: str = ""):
+    """DRAM bytes per launch from a committed ncu summary of the current sources."""
+    return recorded_counter(workload, mode, "dram_bytes_per_launch")
+
+
+def l1_ceiling(w, corner_rows: int, wavefronts, sm_count: int, sm_mhz, launch_s: float,
+               alg_bytes: int, hbm_peak_gbs: float) -> dict:
+    """The SM-side ceiling of the gather: every in-level corner row of every sample passes
+    through an SM's L1 data pipe into registers, which delivers one 128-byte wavefront per
+    SM clock.  rows_floor_us is the time those rows alone need on all SMs at the sampled
+    clock (the minimum of any design that brings each corner row on chip once); floor_us
+    the time of the wavefronts the dominant kernel issued per launch (corner rows plus its
+    tap exchange, loads of locations and weights and stores), from the committed ncu
+    summary of the same sources; frac = that floor over the measured launch time.
+    hbm_frac_ceiling is the HBM-roofline fraction a launch at rows_floor_us would reach."""
+    esize = 2 if w.dtype == "bf16" else 4
+    per_row = max(1, -(-(w.D * esize) // L1_WAVEFRONT_BYTES))
+    rows_wf = corner_rows * per_row
+    if not sm_mhz:
+        return {"bound": "l1_data_pipe", "corner_rows_per_launch": corner_rows, "frac": None}
+    cyc_us = sm_count * float(sm_mhz)                      # wavefronts per microsecond
+    rows_floor = rows_wf / cyc_us
+    floor = wavefronts / cyc_us if wavefronts else None
+    launch_us = launch_s * 1e6
+    return {"bound": "l1_data_pipe", "unit": "wavefronts (128 B; one per SM clock)",
+            "corner_rows_per_launch": corner_rows, "rows_wavefronts_per_launch": rows_wf,
+            "rows_floor_us": rows_floor, "rows_frac": rows_floor / launch_us,
+            "wavefronts_per_launch": wavefronts, "floor_us": floor,
+            "frac": (floor / launch_us) if floor else None,
+            "sm_count": sm_count, "sm_mhz": float(sm_mhz),
+            "hbm_frac_ceiling": alg_bytes / (rows_floor * 1e-6) / 1e9 / hbm_peak_gbs,
+            "source": "rows counted on the host from the inputs; wavefronts from the ncu "
+                      "summary of the current kernel sources (null when none matches)"}
+
+
+def l2_bytes(dev) -> int:
+    """L2 capacity of the device (bytes), as the driver reports it."""
+    import torch
+    return int(torch.cuda.get_device_properties(dev).L2_cache_size)
 
 
 def measured_peaks():
@@ -118,6 +161,12 @@ def measured_peaks():
 def unique_value_rows(w: workloads.Workload, inp) -> int:
     """Distinct (batch, value row, head) rows touched by at least one corner that lies
     inside its level: the value bytes a perfect cache would read once."""
+    return value_row_counts(w, inp)[0]
+
+
+def value_row_counts(w: workloads.Workload, inp):
+    """(distinct rows, all in-level corner rows) of one pass: every in-level corner of
+    every sample brings one D-channel value row of one head on chip."""
     loc = inp["sampling_locations"].astype(np.float64)
     B, Nq, M, L, P, nd = loc.shape
     starts = inp["level_start_index"]
@@ -140,13 +189,15 @@ def unique_value_rows(w: workloads.Workload, inp) -> int:
                 row = (idx[..., 2] * ext[1] + idx[..., 1]) * ext[0] + idx[..., 0]
             gid = ((b_idx * w.Nin + starts[l] + row) * M + m_idx)
             ids.append(gid[inside])
-    return int(np.unique(np.concatenate(ids)).size)
+    allrows = np.concatenate(ids)
+    return int(np.unique(allrows).size), int(allrows.size)
 
 
-def algorithmic_bytes(w: workloads.Workload, inp) -> dict:
+def algorithmic_bytes(w: workloads.Workload, inp, counts=None) -> dict:
+    """Algorithmic bytes of one pass; `counts` = value_row_counts(w, inp) if known."""
     esize = 2 if w.dtype == "bf16" else 4
     row = w.D * esize
-    uniq = unique_value_rows(w, inp) * row
+    uniq = (counts or value_row_counts(w, inp))[0] * row
     loc_b = inp["sampling_locations"].nbytes
     attn_b = inp["attention_weights"].nbytes
     out_b = w.B * w.Nq * w.M * w.D * esize
@@ -424,34 +475,55 @@ def make_step(msda, w, inp, bufs, stream, ordered=False, prune=0.0, fused=False)
 
 
 def cpu_baseline(w, inp, budget_s: float = 10.0, fused: bool = False):
-    """The oracle as it stands (single-threaded C, double precision) on the full workload,
-    repeated until ~budget_s of CPU time; samples per second.  `fused`: the oracle's fused
-    forward / backward on reference points, offsets and logits."""
+    """The oracle as it stands (C, double precision) on the full workload, repeated until
+    about budget_s of wall time; samples per second.  The forward is timed on one host
+    thread and on all of them (the oracle's forward split into blocks of queries, one
+    OpenMP thread each; every output computed as in the serial call); the backward, whose
+    grad_value sums are serial, on one thread.  `fused`: the oracle's fused forward /
+    backward on reference points, offsets and logits."""
     import oracle
     oracle.build()
     args = [np.ascontiguousarray(inp[k], dtype=np.float64) for k in
             ("value", "sampling_locations", "attention_weights")]
     shapes, starts = inp["spatial_shapes"], inp["level_start_index"]
     g = np.ascontiguousarray(inp["grad_out"], dtype=np.float64) if w.backward else None
-    runs, t0 = 0, time.perf_counter()
-    while True:
+
+    def one(threads):
         if fused:
             pro = (inp["reference_points"], inp["sampling_offsets"], inp["attention_logits"])
             if w.backward:
                 oracle.backward_fused(w.ndim, args[0], shapes, starts, *pro, g)
             else:
-                oracle.forward_fused(w.ndim, args[0], shapes, starts, *pro)
+                oracle.forward_fused(w.ndim, args[0], shapes, starts, *pro, threads=threads)
         elif w.backward:
             oracle.backward(w.ndim, args[0], shapes, starts, args[1], args[2], g)
         else:
-            oracle.forward(w.ndim, args[0], shapes, starts, args[1], args[2])
-        runs += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    return {"value": w.samples * runs / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{runs} full pass(es) of the {w.name} workload "
-                      f"({w.samples} samples each), {el:.1f} s, 1 thread, fp64"}
+            oracle.forward(w.ndim, args[0], shapes, starts, args[1], args[2], threads=threads)
+
+    def timed(threads, budget):
+        runs, t0 = 0, time.perf_counter()
+        while True:
+            one(threads)
+            runs += 1
+            el = time.perf_counter() - t0
+            if el >= budget:
+                return runs, el
+
+    what = f"the {w.name} workload ({w.samples} samples each)"
+    if w.backward:
+        runs, el = timed(1, budget_s)
+        return {"value": w.samples * runs / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{runs} full pass(es) of {what}, {el:.1f} s, 1 thread (the "
+                          "backward's grad_value sums are serial), fp64"}
+    n_all = oracle.default_threads()
+    r1, e1 = timed(1, budget_s / 2)
+    rn, en = timed(0, budget_s / 2)
+    return {"value": w.samples * rn / en, "unit": UNIT, "cores": n_all, "kind": "oracle",
+            "sample": f"{rn} full pass(es) of {what}, {en:.1f} s, {n_all} threads (OpenMP "
+                      "over blocks of 64 queries), fp64",
+            "single_core": {"value": w.samples * r1 / e1, "unit": UNIT, "cores": 1,
+                            "sample": f"{r1} full pass(es), {e1:.1f} s, 1 thread"},
+            "host_cpus": os.cpu_count()}
 
 
 def run_ours(args):
@@ -481,7 +553,8 @@ def run_ours(args):
     set_bytes += w.B * w.Nq * w.M * w.D * esize
     if w.backward:
         set_bytes += base["value"].numel() * 4 + base["loc"].numel() * 4 + base["attn"].numel() * 4
-    n_sets = max(2, int(np.ceil(2 * L2_BYTES / set_bytes)) + 1)
+    l2 = l2_bytes(dev)
+    n_sets = max(2, int(np.ceil(2 * l2 / set_bytes)) + 1)
     bufs = []
     for i in range(n_sets):
         b = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
@@ -520,20 +593,35 @@ def run_ours(args):
         graph.replay()
     torch.cuda.synchronize(dev)
 
+    # Pre-heat: the step graph replayed untimed for about half a second, so that the timed
+    # replays start from steady clocks and power state (a few milliseconds of work right
+    # after an idle period measured 10-20% slower per step than the steady state).
+    t_heat = time.perf_counter()
+    while time.perf_counter() - t_heat < args.preheat_s:
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+
+    # Timed: `replays` separate timings of exactly K steps (one replay of the K-step graph
+    # each), every one bracketed by a barrier and a device synchronize; the reported time
+    # is the median of the per-rank maxima.  Clocks are sampled over all of them.
     clocks = ClockSampler(local, pci_bus_id(dev))
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
+    t_replays = []
     with clocks:
-        ev0.record(stream)
-        with torch.cuda.stream(stream):
-            graph.replay()
-        ev1.record(stream)
-        clocks.sample_once()
-        torch.cuda.synchronize(dev)
-    barrier(world)
-    t_rank = ev0.elapsed_time(ev1) / 1e3                      # seconds, this rank
+        for _ in range(args.replays):
+            barrier(world)
+            torch.cuda.synchronize(dev)
+            ev0.record(stream)
+            with torch.cuda.stream(stream):
+                graph.replay()
+            ev1.record(stream)
+            clocks.sample_once()
+            torch.cuda.synchronize(dev)
+            barrier(world)
+            t_replays.append(all_max(ev0.elapsed_time(ev1) / 1e3, world))
+    t_rank = statistics.median(t_replays)                     # seconds (max over ranks)
     value, t_max = aggregate(t_rank, w.samples, args.steps, world)
     ms_per_step = t_max * 1e3 / args.steps
 
@@ -561,7 +649,9 @@ def run_ours(args):
     if rank != 0:
         barrier(world)
         return None
-    ab = algorithmic_bytes(w, fused_byte_inputs(w, inp) if args.fused else inp)
+    byte_inp = fused_byte_inputs(w, inp) if args.fused else inp
+    counts = value_row_counts(w, byte_inp)
+    ab = algorithmic_bytes(w, byte_inp, counts)
     if args.fused:
         ref_b = inp["reference_points"].nbytes
         ab["total"] += ref_b
@@ -572,30 +662,28 @@ def run_ours(args):
     peak, peak_src = measured_peaks()
     per_launch_s = t_rank / args.steps
     achieved = ab["total"] / per_launch_s / 1e9
-    traffic = recorded_traffic(w.name, "+order" if args.order else "+fused" if args.fused else
-                               f"+prune{args.prune:g}" if args.prune > 0 else "")
+    mode = ("+order" if args.order else "+fused" if args.fused else
+            f"+prune{args.prune:g}" if args.prune > 0 else "")
+    traffic = recorded_traffic(w.name, mode)
+    clk = clocks.summary()
+    secondary = l1_ceiling(w, counts[1], recorded_counter(w.name, mode, "l1_wavefronts_per_launch"),
+                           torch.cuda.get_device_properties(dev).multi_processor_count,
+                           clk.get("sm_mhz") or clk.get("sm_max_mhz"), per_launch_s,
+                           ab["total"], peak)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
-        "config": {**workload_config(w),
-                   "query_order": "computed each step (msda_query_order) and used by the "
-                                  "ordered forward" if args.order else "as given",
-                   "prologue": ("fused: reference points + pixel offsets + logits in, "
-                                "softmax and locations in the kernel") if args.fused
-                               else "none: locations and weights given",
-                   "prune": (f"samples with |A| < {args.prune} skipped "
-                             f"({float((np.abs(inp['attention_weights']) < args.prune).mean()):.3f}"
-                             " of them): an approximation") if args.prune > 0 else "none (exact)",
-                   "l2": f"cold: {n_sets} rotating input sets of {set_bytes / 1e6:.1f} MB "
-                         f"(> 2x L2) between steps",
-                   "parallelism": f"weak: {world} rank(s), one batch each, no collective"},
+        "config": run_config(w, args, world),
+        "l2_rotation": f"{n_sets} rotating input sets of {set_bytes / 1e6:.1f} MB against "
+                       f"{l2 / 2**20:.0f} MiB of L2",
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.4 TB/s",
+                     "secondary": secondary,
                      "nominal": {"peak": NOMINAL_HBM_GBS, "frac": achieved / NOMINAL_HBM_GBS,
                                  "note": "HBM3e nominal, the metric's ~8 TB/s"},
                      "algorithmic_bytes_per_launch": ab["total"],
@@ -610,7 +698,10 @@ def run_ours(args):
                     "value": w.samples * n_warm / t_warm, "unit": UNIT, "steps": n_warm,
                     "note": "rank 0; one input set back to back, outside the timed region"},
         "gpu_launches": args.steps * launches_per_step,
-        "clocks": clocks.summary(),
+        "clocks": clk,
+        "timing": {"replays": args.replays, "preheat_s": args.preheat_s,
+                   "ms_per_step_each": [t * 1e3 / args.steps for t in t_replays],
+                   "note": "each replay times exactly K steps; ms_per_step is the median"},
         "kernel_source_sha256": kernel_source_hash("backward" if w.backward else "forward"),
     }
     if e2e is not None:
@@ -716,6 +807,22 @@ def run_e2e(msda, w, inp, dev, args, world):
 # ----------------------------------------------------------------------------- reference arm
 
 
+def run_config(w: workloads.Workload, args, world: int) -> dict:
+    """The JSON line's `config`: the workload, the mode of the step and how the timing
+    treats L2.  Both arms print the same dict for the same command-line flags."""
+    return {**workload_config(w),
+            "query_order": ("computed each step (msda_query_order) and used by the "
+                            "ordered forward") if args.order else "as given",
+            "prologue": ("fused: reference points + pixel offsets + logits in, "
+                         "softmax and locations in the kernel") if args.fused
+                        else "none: locations and weights given",
+            "prune": (f"samples with |A| < {args.prune} skipped: an approximation"
+                      if args.prune > 0 else "none (exact)"),
+            "l2": "cold: the inputs of consecutive steps rotate over more than twice the "
+                  "GPU's L2 capacity",
+            "parallelism": f"weak: {world} rank(s), one batch each, no collective"}
+
+
 def workload_config(w: workloads.Workload) -> dict:
     """The workload keys of the JSON line's `config`, the same on both arms."""
     return {"workload": w.name, "B": w.B, "Nin": w.Nin, "Nq": w.Nq, "M": w.M, "D": w.D,
@@ -749,17 +856,27 @@ def run_reference(args):
                        f["attention_logits"][:1])
         value = np.ascontiguousarray(f["value"][:1], dtype=np.float64)
 
+    # the forward on every host thread (the oracle's block split over OpenMP threads); the
+    # backward's grad_value sums are serial, so it runs on one
+    threads = 1 if w.backward else 0
+    cores = 1 if w.backward else oracle.default_threads()
+
     def run(q0, q1):
         sl = slice(q0, q1)
         if args.fused and w.backward:
             oracle.backward_fused(w.ndim, value, shapes, starts, ref[:, sl], off[:, sl],
                                   z[:, sl], g[:, sl])
         elif args.fused:
-            oracle.forward_fused(w.ndim, value, shapes, starts, ref[:, sl], off[:, sl], z[:, sl])
+            oracle.forward_fused(w.ndim, value, shapes, starts, ref[:, sl], off[:, sl], z[:, sl],
+                                 threads=threads)
         elif w.backward:
             oracle.backward(w.ndim, value, shapes, starts, loc[:, sl], attn[:, sl], g[:, sl])
+        elif args.prune > 0:
+            oracle.forward_pruned(w.ndim, value, shapes, starts, loc[:, sl], attn[:, sl],
+                                  args.prune, threads=threads)
         else:
-            oracle.forward(w.ndim, value, shapes, starts, loc[:, sl], attn[:, sl])
+            oracle.forward(w.ndim, value, shapes, starts, loc[:, sl], attn[:, sl],
+                           threads=threads)
 
     # calibrate: size one step to ~min(0.5 s, 90 s / (K + W))
     nq = min(w.Nq, 256)
@@ -778,21 +895,21 @@ def run_reference(args):
     el = time.perf_counter() - t0
     v = nq * per_q * args.steps / el
     sample = (f"each step: queries [q0, q0+{nq}) of batch 0 of the {w.name} workload "
-              f"({nq * per_q} samples), all heads/levels/points; 1 thread, fp64 oracle"
+              f"({nq * per_q} samples), all heads/levels/points; {cores} thread(s), fp64 oracle"
               + ("; fused prologue (reference points, offsets, logits)" if args.fused else ""))
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w),
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "config": run_config(w, args, world),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
 
-def main(argv=None):
+def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
@@ -809,11 +926,21 @@ def main(argv=None):
     ap.add_argument("--prune", type=float, default=0.0,
                     help="forward workloads: skip samples with |A| below this threshold "
                          "(approximate; 0 = exact)")
+    ap.add_argument("--replays", type=int, default=5,
+                    help="timed replays of the K-step graph (each exactly K steps); the "
+                         "median is reported")
+    ap.add_argument("--preheat-s", type=float, default=0.5,
+                    help="seconds of untimed replays before the timed ones")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline leg")
+    return ap
+
+
+def main(argv=None):
+    ap = build_parser()
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -22,9 +22,19 @@ import workloads  # noqa: E402
 
 
 def _brute_unique_rows(inp):
+    return len(set(_brute_rows(inp)))
+
+
+def _brute_corner_rows(inp):
+    return len(_brute_rows(inp))
+
+
+def _brute_rows(inp):
+    """Every (batch, value row, head) an in-level corner of a sample touches, with
+    repeats, one sample and one corner at a time."""
     loc = inp["sampling_locations"].astype(np.float64)
     B, Nq, M, L, P, nd = loc.shape
-    rows = set()
+    rows = []
     for b in range(B):
         for q in range(Nq):
             for m in range(M):
@@ -43,8 +53,8 @@ def _brute_unique_rows(inp):
                             flat = idx[0] + ext[0] * idx[1]
                             if nd == 3:
                                 flat += ext[0] * ext[1] * idx[2]
-                            rows.add((b, start + flat, m))
-    return len(rows)
+                            rows.append((b, start + flat, m))
+    return rows
 
 
 @pytest.mark.parametrize("nd,shapes", [(2, [(7, 9), (3, 4)]), (3, [(3, 4, 5), (2, 2, 3)])])
@@ -97,16 +107,39 @@ def _run_bench(args, env_extra=None):
 def test_reference_arm_prints_one_contract_line():
     """`bench.py --impl reference` (the CPU oracle, no GPU) prints one JSON line with the
     contract's keys, on the same metric and workload keys as the GPU arm."""
-    (line,) = _run_bench(["--impl", "reference", "--workload", "tiny2d", "--steps", "3",
-                          "--warmup", "3"])
+    flags = ["--workload", "tiny2d", "--steps", "3", "--warmup", "3"]
+    (line,) = _run_bench(["--impl", "reference", *flags])
     for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
               "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
               "impl", "cpu_baseline", "e2e", "gpu_launches"):
         assert k in line, k
     assert line["impl"] == "reference" and line["metric"] == bench.METRIC
     assert line["value"] > 0 and line["steps"] == 3 and line["gpu_launches"] == 0
-    assert line["config"] == bench.workload_config(workloads.WORKLOADS["tiny2d"])
-    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["cores"] == 1
+    # the same config dict as the GPU arm prints for the same flags
+    args = bench.build_parser().parse_args(flags)
+    assert line["config"] == bench.run_config(workloads.WORKLOADS["tiny2d"], args, 1)
+    # the forward oracle runs on every host thread
+    import oracle
+    oracle.build()
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["cores"] == oracle.default_threads()
+
+
+def test_corner_row_count_and_l1_ceiling():
+    """The L1 ceiling counts every in-level corner row of every sample (brute force on a
+    small problem) and turns rows into microseconds at one 128-B wavefront per SM clock."""
+    nd, shapes = 2, [(5, 7), (2, 3)]
+    inp = workloads.random_problem(nd, shapes, B=2, Nq=9, M=3, D=8, P=2, seed=5,
+                                   backward=False)
+    w = workloads.Workload("t", nd, 2, tuple(shapes), 9, 3, 8, 2, "f32", 5)
+    uniq, total = bench.value_row_counts(w, inp)
+    assert uniq == _brute_unique_rows(inp)
+    assert total == _brute_corner_rows(inp)
+    c = bench.l1_ceiling(w, 148 * 2000 * 10, None, 148, 2000.0, 20e-6, 6.4e6, 6400.0)
+    assert abs(c["rows_floor_us"] - 10.0) < 1e-9 and abs(c["rows_frac"] - 0.5) < 1e-12
+    assert c["frac"] is None and abs(c["hbm_frac_ceiling"] - 0.1) < 1e-12
+    c = bench.l1_ceiling(w, 1, 148 * 2000 * 15, 148, 2000.0, 20e-6, 6.4e6, 6400.0)
+    assert abs(c["floor_us"] - 15.0) < 1e-9 and abs(c["frac"] - 0.75) < 1e-12
 
 
 def test_reference_arm_other_ranks_stay_silent():
