@@ -413,11 +413,13 @@ def fused_byte_inputs(w, f):
                 attention_weights=f["attention_logits"])
 
 
-def make_step(msda, w, inp, bufs, stream, ordered=False, prune=0.0, fused=False):
+def make_step(msda, w, inp, bufs, stream, ordered=None, prune=0.0, fused=False):
     """Returns step(i): one pass of the hot path on input set i % len(bufs).  With
-    `ordered`, each step first computes the locality-aware query order of its input set
-    (msda_query_order) and then runs the ordered forward, both inside the step.  With
-    `prune` > 0 it runs the pruned forward (samples with |A| < prune skipped)."""
+    ordered = "step", each step first computes the locality-aware query order of its input
+    set (msda_query_order) and then runs the ordered forward, both inside the step; with
+    "once", the order of every input set is computed here, before any timing, and the step
+    runs only the ordered forward.  With `prune` > 0 it runs the pruned forward (samples
+    with |A| < prune skipped)."""
     shapes, starts = inp["spatial_shapes"], inp["level_start_index"]
     if fused and w.backward:
         fn = msda.msda2d_backward_fused if w.ndim == 2 else msda.msda3d_backward_fused
@@ -445,6 +447,18 @@ def make_step(msda, w, inp, bufs, stream, ordered=False, prune=0.0, fused=False)
         def step(i):
             b = bufs[i % len(bufs)]
             fn(b["value"], shapes, starts, b["loc"], b["attn"], prune, out=b["out"],
+               stream=stream)
+        return step, 1
+    if ordered == "once":
+        fn = msda.msda2d_forward_ordered if w.ndim == 2 else msda.msda3d_forward_ordered
+        with __import__("torch").cuda.stream(stream):
+            for b in bufs:
+                msda.msda_query_order(b["loc"], query_order=b["order"], workspace=b["ws"],
+                                      stream=stream)
+
+        def step(i):
+            b = bufs[i % len(bufs)]
+            fn(b["value"], shapes, starts, b["loc"], b["attn"], b["order"], out=b["out"],
                stream=stream)
         return step, 1
     if ordered:
@@ -662,7 +676,8 @@ def run_ours(args):
     peak, peak_src = measured_peaks()
     per_launch_s = t_rank / args.steps
     achieved = ab["total"] / per_launch_s / 1e9
-    mode = ("+order" if args.order else "+fused" if args.fused else
+    mode = ("+order" if args.order == "step" else "+order_once" if args.order == "once" else
+            "+fused" if args.fused else
             f"+prune{args.prune:g}" if args.prune > 0 else "")
     traffic = recorded_traffic(w.name, mode)
     clk = clocks.summary()
@@ -688,7 +703,9 @@ def run_ours(args):
                                  "note": "HBM3e nominal, the metric's ~8 TB/s"},
                      "algorithmic_bytes_per_launch": ab["total"],
                      "bytes_breakdown": ab["parts"],
-                     "kernel": ("query order + ordered msda fwd" if args.order else
+                     "kernel": ("query order + ordered msda fwd" if args.order == "step" else
+                                "ordered msda fwd (order computed once per input set)"
+                                if args.order == "once" else
                                 "pruned msda fwd" if args.prune > 0 else
                                 "fused-prologue msda fwd" if args.fused else "msda fwd")
                                if not w.backward else
@@ -811,8 +828,11 @@ def run_config(w: workloads.Workload, args, world: int) -> dict:
     """The JSON line's `config`: the workload, the mode of the step and how the timing
     treats L2.  Both arms print the same dict for the same command-line flags."""
     return {**workload_config(w),
-            "query_order": ("computed each step (msda_query_order) and used by the "
-                            "ordered forward") if args.order else "as given",
+            "query_order": {"step": "computed each step (msda_query_order) and used by the "
+                                    "ordered forward",
+                            "once": "computed once per input set before the timed region "
+                                    "(msda_query_order); each step runs the ordered forward",
+                            None: "as given"}[args.order],
             "prologue": ("fused: reference points + pixel offsets + logits in, "
                          "softmax and locations in the kernel") if args.fused
                         else "none: locations and weights given",
@@ -916,9 +936,13 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=workloads.names(), default="encoder2d")
-    ap.add_argument("--order", action="store_true",
-                    help="forward workloads: compute the locality-aware query order inside "
-                         "each step and run the ordered forward")
+    ap.add_argument("--order", nargs="?", const="step", default=None,
+                    choices=["step", "once"],
+                    help="forward workloads: run the ordered forward with the locality-aware "
+                         "query order computed inside each step ('step', the default), or "
+                         "computed once per input set before the timed region ('once': an "
+                         "encoder's layers share their reference points and can share one "
+                         "order)")
     ap.add_argument("--fused", action="store_true",
                     help="reference points, pixel offsets and logits in; the kernel forms "
                          "locations and the softmax (backward workloads: the fused backward, "

@@ -278,4 +278,67 @@ __device__ __forceinline__ Taps<4> shfl_taps_packed(const Taps<4> &t, int src, i
     return r;
 }
 
+// ------------------------------------------------------------------ value-row slices
+
+// VB bytes of one value row held by one lane (16: one 128-bit load; 32: one 256-bit load).
+template <int VB> struct Slice;
+template <> struct Slice<16> { uint4 a; };
+template <> struct Slice<32> { uint4 a, b; };
+
+__device__ __forceinline__ void load_slice(const char *p, Slice<16> &r) { r.a = ldg16(p); }
+__device__ __forceinline__ void load_slice(const char *p, Slice<32> &r) { ldg32(p, r.a, r.b); }
+__device__ __forceinline__ void zero_slice(Slice<16> &r) { r.a = make_uint4(0, 0, 0, 0); }
+__device__ __forceinline__ void zero_slice(Slice<32> &r) {
+    r.a = make_uint4(0, 0, 0, 0);
+    r.b = r.a;
+}
+
+// Shared-memory slot of sample s of an item's tap records: one pad slot after every 8, so
+// that the 8 lanes of a group writing their samples' records (two consecutive samples
+// each) hit distinct banks.
+__host__ __device__ constexpr int tap_slot(int s) { return s + (s >> 3); }
+
+// Corner data ("tap record") of one sample, as the lane that computed it leaves it in
+// shared memory for the other lanes of its group (forward and backward): x = value row of
+// corner 0 (int bits; the forward may carry the validity bits under it), y = attention
+// weight a, z / w = fractions fx / fy; 3D adds fz (and the validity bits when not packed)
+// in second arrays.  A reader forms the corner weights from (a, fx, fy[, fz]) with
+// tap_weights, the same expressions as make_taps, so its weights are bit-identical to the
+// owner's.  Four words instead of the four weights: one shared-memory wavefront less per
+// warp step in 2D.
+template <int NC> struct TapView {
+    int row;
+    unsigned ok;
+    float w[NC];
+};
+
+__device__ __forceinline__ void tap_weights(float a, float fx, float fy, float (&w)[4]) {
+    const float ay0 = a * (1.f - fy), ay1 = a * fy;
+    w[0] = ay0 * (1.f - fx);
+    w[1] = ay0 * fx;
+    w[2] = ay1 * (1.f - fx);
+    w[3] = ay1 * fx;
+}
+__device__ __forceinline__ void tap_weights(float a, float fx, float fy, float fz, float (&w)[8]) {
+    const float wx[2] = {1.f - fx, fx};
+    const float wy[2] = {1.f - fy, fy};
+    const float wz[2] = {a * (1.f - fz), a * fz};
+#pragma unroll
+    for (int c = 0; c < 8; ++c) w[c] = (wz[c >> 2] * wy[(c >> 1) & 1]) * wx[c & 1];
+}
+
+// Slice load under a predicate, without zeroing: when `pred` is false the destination
+// holds an unspecified value and the caller must not read it (the matching FMAs are under
+// the same predicate).  The empty asm gives the compiler a value to start from that costs
+// no instruction; the load itself stays behind the branch.
+__device__ __forceinline__ void load_slice_if(bool pred, const char *p, Slice<16> &r) {
+    asm("" : "=r"(r.a.x), "=r"(r.a.y), "=r"(r.a.z), "=r"(r.a.w));
+    if (pred) r.a = ldg16(p);
+}
+__device__ __forceinline__ void load_slice_if(bool pred, const char *p, Slice<32> &r) {
+    asm("" : "=r"(r.a.x), "=r"(r.a.y), "=r"(r.a.z), "=r"(r.a.w), "=r"(r.b.x), "=r"(r.b.y),
+             "=r"(r.b.z), "=r"(r.b.w));
+    if (pred) ldg32(p, r.a, r.b);
+}
+
 }  // namespace msda

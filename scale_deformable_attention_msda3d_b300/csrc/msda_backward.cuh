@@ -14,10 +14,12 @@
 //   lanes / wider rows, which differ only in the residency they ask of the compiler).  A CTA handles one (batch, head) and a run of
 //   queries; a lane group of G lanes (16 bytes of channels each) handles one query.  Lane
 //   j of the group owns samples j, G + j, 2G + j, ...: it reads their locations and
-//   weights and computes their taps, which the group takes by shuffle.  Every lane forms
-//   its partial dot products <g, v_c> over its channels; after each batch of G samples a
-//   butterfly reduce-scatter leaves each sample's full dot products on its owner, which
-//   writes grad_A and grad_loc.  grad_value goes through 16-byte red.global.add.v4.f32.
+//   weights, computes their taps and leaves each sample's tap record (row, a, fractions,
+//   validity bits) in shared memory for the group.  Every lane loads the in-level corner
+//   rows of each sample (predicated, no zeroed registers) and forms its partial dot
+//   products <g, v_c> over its channels; after each batch of G samples a butterfly
+//   reduce-scatter leaves each sample's full dot products on its owner, which writes grad_A
+//   and grad_loc.  grad_value goes through 16-byte red.global.add.v4.f32.
 //   (Accumulating small levels in shared memory first was measured and dropped: on this
 //   part shared-memory fp32 atomics ran about ten times slower than the L2 reductions.)
 // * bwd{2,3}d_generic (any L, P): every lane of the group computes every sample, reduces
@@ -292,11 +294,19 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
 
     const char *vbase = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
                         static_cast<long long>(m) * (rb / p.M) + sub * 16;
-    float *gbase = p.grad_value + (b * p.Nin) * rowf + static_cast<long long>(m) * D + sub * N;
-    const int rounds = static_cast<int>((q_hi - q_lo + GPB - 1) / GPB);
+    constexpr int GS = 4 / Vec<DT>::ESIZE;  // grad_value (fp32) bytes per value byte
+    char *gbase = reinterpret_cast<char *>(p.grad_value + (b * p.Nin) * rowf +
+                                           static_cast<long long>(m) * D + sub * N);
+    // tap records of the CTA's queries (see common.cuh): row, a, fx, fy (+ fz), validity
+    constexpr int ISTR = tap_slot(S - 1) + 2;
+    constexpr int OKB = NDIM == 2 ? 4 : 8;  // validity bits under a packed row
+    __shared__ float4 rec[GPB * ISTR];
+    __shared__ unsigned rec_ok[GPB * ISTR];
+    __shared__ float rec_z[NDIM == 3 ? GPB * ISTR : 1];
 
-    for (int r = 0; r < rounds; ++r) {
-        long long q = q_lo + static_cast<long long>(r) * GPB + grp;
+    {
+        // one lane group per query: the launch makes a CTA's query run exactly GPB long
+        long long q = q_lo + grp;
         const bool active = q < q_hi;
         if (!active) q = q_hi - 1;  // recompute a real query, write nothing
         const long long item = (b * p.Nq + q) * p.M + m;
@@ -327,15 +337,24 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
             for (int bt = 0; bt < NB; ++bt) av[bt] = __fdiv_rn(av[bt], sum);
         }
 
+        // 1. taps of the samples this lane owns (bt * G + sub), kept for the owner's
+        //    gradient formulas and left in shared memory for the group
+        float frac[NB][NDIM], aw[NB];
+        unsigned okw[NB];
 #pragma unroll
         for (int bt = 0; bt < NB; ++bt) {
-            // taps of the sample this lane owns in this batch
             const int own = bt * G + sub;
-            const bool owns = own < S;
-            const int so = owns ? own : S - 1;
+            const int so = own < S ? own : S - 1;
             float xyz[NDIM];
+            const float *lsrc = p.loc + (item * S + so) * NDIM;
+            if constexpr (NDIM == 2) {
+                const float2 v = __ldcs(reinterpret_cast<const float2 *>(lsrc));
+                xyz[0] = v.x;
+                xyz[1] = v.y;
+            } else {
 #pragma unroll
-            for (int k = 0; k < NDIM; ++k) xyz[k] = __ldcs(p.loc + (item * S + so) * NDIM + k);
+                for (int k = 0; k < NDIM; ++k) xyz[k] = __ldcs(lsrc + k);
+            }
             float a;
             if constexpr (FUSED) {
 #pragma unroll
@@ -346,9 +365,27 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
                 a = __ldcs(p.attn + item * S + so);
             }
             Taps<NC> mine;
-            float frac[NDIM];
-            make_taps(p, so / PP, xyz, a, mine, frac);
+            make_taps(p, so / PP, xyz, a, mine, frac[bt]);
+            aw[bt] = a;
+            okw[bt] = mine.ok;
+            if (own < S) {
+                // the validity bits ride under the row when it leaves room (p.pack_taps)
+                const int j = grp * ISTR + tap_slot(own);
+                const int rbits =
+                    p.pack_taps ? static_cast<int>((static_cast<unsigned>(mine.row) << OKB) | mine.ok)
+                                : mine.row;
+                rec[j] = make_float4(__int_as_float(rbits), a, frac[bt][0], frac[bt][1]);
+                if (!p.pack_taps) rec_ok[j] = mine.ok;
+                if constexpr (NDIM == 3) rec_z[j] = frac[bt][2];
+            }
+        }
+        __syncwarp();
 
+        // 2. per batch of G samples: corner rows (in-level corners only), partial dot
+        //    products <g, v_c> over this lane's channels, grad_value reductions; then the
+        //    owner of each sample gets its full dot products and writes grad_A, grad_loc
+#pragma unroll
+        for (int bt = 0; bt < NB; ++bt) {
             float dp[G][NC];  // partial <g, v_c> of every sample of the batch
 #pragma unroll
             for (int j = 0; j < G; ++j) {
@@ -358,39 +395,54 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
                     for (int c = 0; c < NC; ++c) dp[j][c] = 0.f;
                     continue;
                 }
-                const Taps<NC> t = shfl_taps(mine, j, G);
+                const int jr = grp * ISTR + tap_slot(s);
+                const float4 rr = rec[jr];
+                const int rv = __float_as_int(rr.x);
+                const int row = p.pack_taps ? rv >> OKB : rv;
+                const unsigned ok = p.pack_taps ? static_cast<unsigned>(rv) & ((1u << OKB) - 1u)
+                                                : rec_ok[jr];
+                float w[NC];
+                if constexpr (NDIM == 2) tap_weights(rr.y, rr.z, rr.w, w);
+                else tap_weights(rr.y, rr.z, rr.w, rec_z[jr], w);
                 const int l = s / PP;
-                const char *c0 = vbase + static_cast<long long>(t.row) * p.rb32;
+                // value and grad_value addresses of corner 0 and of the corner one image row
+                // further; grad_value rows are fp32, GS times as wide as value rows
+                const char *c0 = vbase + static_cast<long long>(row) * p.rb32;
+                const char *cy[2] = {c0, c0 + p.sy[l]};
+                char *g0 = gbase + static_cast<long long>(row) * (static_cast<long long>(p.rb32) * GS);
+                char *gy[2] = {g0, g0 + p.sy[l] * GS};
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
-                    long long off = dx ? rb : 0;
-                    if (dy) off += p.sy[l];
-                    if (dz) off += p.sz[l];
-                    uint4 u = make_uint4(0, 0, 0, 0);
-                    const bool in = (t.ok >> c) & 1u;
-                    if (in) u = ldg16(c0 + off);
+                    const bool in = (ok >> c) & 1u;
+                    const char *src = cy[dy] + (dz ? p.sz[l] : 0) + (dx ? rb : 0);
+                    Slice<16> u;
+                    load_slice_if(in, src, u);
                     float v[N];
-                    unpack(u, v);
+                    unpack(u.a, v);
                     float d = 0.f;
+                    if (in) {
 #pragma unroll
-                    for (int i = 0; i < N; ++i) d = fmaf(g[i], v[i], d);
+                        for (int i = 0; i < N; ++i) d = fmaf(g[i], v[i], d);
+                    }
                     dp[j][c] = d;
                     if (active && in) {
-                        const int crow = t.row + dx + (dy ? p.W[l] : 0) + (dz ? p.W[l] * p.H[l] : 0);
-                        add_global<N>(gbase + static_cast<long long>(crow) * rowf, t.w[c], g);
+                        char *dst = gy[dy] + (dz ? p.sz[l] * GS : 0) + (dx ? rb * GS : 0);
+                        add_global<N>(reinterpret_cast<float *>(dst), w[c], g);
                     }
                 }
             }
             reduce_scatter<G, NC>(dp, sub);
-            if (active && owns) {
+            const int own = bt * G + sub;
+            if (active && own < S) {
                 // dp[0][c] = <g, v_c> of sample `own`; corner weight derivatives from frac
                 const long long s = item * S + own;
+                const float *fr = frac[bt];
                 float wx[2], wy[2], wz[2];
-                wx[0] = 1.f - frac[0]; wx[1] = frac[0];
-                wy[0] = 1.f - frac[1]; wy[1] = frac[1];
+                wx[0] = 1.f - fr[0]; wx[1] = fr[0];
+                wy[0] = 1.f - fr[1]; wy[1] = fr[1];
                 wz[0] = 1.f; wz[1] = 1.f;
-                if constexpr (NDIM == 3) { wz[0] = 1.f - frac[2]; wz[1] = frac[2]; }
+                if constexpr (NDIM == 3) { wz[0] = 1.f - fr[2]; wz[1] = fr[2]; }
                 float gA = 0.f, gx = 0.f, gy = 0.f, gz = 0.f;
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
@@ -402,8 +454,9 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
                     gy = fmaf(sy * wz[dz] * wx[dx], d, gy);
                     if constexpr (NDIM == 3) gz = fmaf(sz * wy[dy] * wx[dx], d, gz);
                 }
-                const bool any = mine.ok != 0u;
+                const bool any = okw[bt] != 0u;
                 const int l = own / PP;
+                const float a = aw[bt];
                 // fused: the offset gradient, d location / d offset = 1 / extent
                 if constexpr (FUSED) gAs[bt] = gA;
                 else p.grad_attn[s] = gA;
@@ -460,7 +513,8 @@ template <int NDIM> constexpr int bwd_block() { return NDIM == 3 ? 128 : 256; }
 template <int DT, int G, int NDIM, int LL, int PP, bool FUSED>
 cudaError_t launch_bwd_tiled(Params p, cudaStream_t s) {
     constexpr int BT = bwd_block<NDIM>();
-    // one round of lane groups per CTA: CTA = (b, m, run of BT / G queries)
+    // one lane group per query, one round per CTA: CTA = (b, m, run of BT / G queries)
+    // (bwd_tiled_body relies on qchunk == BT / G)
     p.qchunk = BT / G;
     p.nchunk = static_cast<int>((p.Nq + p.qchunk - 1) / p.qchunk);
     const long long ctas = p.B * p.M * p.nchunk;

@@ -191,19 +191,6 @@ fwd3d_generic(const __grid_constant__ Params p) {
 
 // ------------------------------------------------------------------ compiled (L, P)
 
-// VB bytes of one value row held by one lane (16: one 128-bit load; 32: one 256-bit load).
-template <int VB> struct Slice;
-template <> struct Slice<16> { uint4 a; };
-template <> struct Slice<32> { uint4 a, b; };
-
-__device__ __forceinline__ void load_slice(const char *p, Slice<16> &r) { r.a = ldg16(p); }
-__device__ __forceinline__ void load_slice(const char *p, Slice<32> &r) { ldg32(p, r.a, r.b); }
-__device__ __forceinline__ void zero_slice(Slice<16> &r) { r.a = make_uint4(0, 0, 0, 0); }
-__device__ __forceinline__ void zero_slice(Slice<32> &r) {
-    r.a = make_uint4(0, 0, 0, 0);
-    r.b = r.a;
-}
-
 // acc += w * (the channels of one 16-byte piece), packed fp32x2 FMAs (same rounding as fmaf).
 template <int DT>
 __device__ __forceinline__ void fma16(float2 *acc, float w, const uint4 &u) {
@@ -253,53 +240,6 @@ template <> struct Shape<2, kBF16> { static constexpr int VB = 16, AHEAD = 1, MI
 template <> struct Shape<3, kF32> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; static constexpr bool PRED = false; };
 template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; static constexpr bool PRED = false; };
 
-// Shared-memory slot of sample s of an item: one pad slot after every 8, so that the 8
-// lanes of a group writing their samples' records (two consecutive samples each) hit
-// distinct banks.
-__host__ __device__ constexpr int tap_slot(int s) { return s + (s >> 3); }
-
-// Corner data ("tap record") of one sample, as the lane that computed it leaves it in
-// shared memory for the other lanes of its group: rec.x = value row of corner 0 (int bits;
-// with PACK the validity bits sit under it), rec.y = attention weight a, rec.z / rec.w =
-// fractions fx / fy; 3D adds fz (and the validity bits when not packed) in a second array.
-// A reader forms the corner weights from (a, fx, fy[, fz]) with the same expressions as
-// make_taps, so its weights are bit-identical to the owner's.  Four words instead of the
-// four weights: one shared-memory wavefront less per warp step.
-template <int NC> struct TapView {
-    int row;
-    unsigned ok;
-    float w[NC];
-};
-
-__device__ __forceinline__ void tap_weights(float a, float fx, float fy, float (&w)[4]) {
-    const float ay0 = a * (1.f - fy), ay1 = a * fy;
-    w[0] = ay0 * (1.f - fx);
-    w[1] = ay0 * fx;
-    w[2] = ay1 * (1.f - fx);
-    w[3] = ay1 * fx;
-}
-__device__ __forceinline__ void tap_weights(float a, float fx, float fy, float fz, float (&w)[8]) {
-    const float wx[2] = {1.f - fx, fx};
-    const float wy[2] = {1.f - fy, fy};
-    const float wz[2] = {a * (1.f - fz), a * fz};
-#pragma unroll
-    for (int c = 0; c < 8; ++c) w[c] = (wz[c >> 2] * wy[(c >> 1) & 1]) * wx[c & 1];
-}
-
-// Slice load under a predicate, without zeroing: when `pred` is false the destination
-// holds an unspecified value and the caller must not read it (the matching FMAs are under
-// the same predicate).  The empty asm gives the compiler a value to start from that costs
-// no instruction; the load itself stays behind the branch.
-__device__ __forceinline__ void load_slice_if(bool pred, const char *p, Slice<16> &r) {
-    asm("" : "=r"(r.a.x), "=r"(r.a.y), "=r"(r.a.z), "=r"(r.a.w));
-    if (pred) r.a = ldg16(p);
-}
-__device__ __forceinline__ void load_slice_if(bool pred, const char *p, Slice<32> &r) {
-    asm("" : "=r"(r.a.x), "=r"(r.a.y), "=r"(r.a.z), "=r"(r.a.w), "=r"(r.b.x), "=r"(r.b.y),
-             "=r"(r.b.z), "=r"(r.b.w));
-    if (pred) ldg32(p, r.a, r.b);
-}
-
 // One item = (b, q, m); LANES = G * SPLIT lanes per item; lane = (item, sp, sub).
 // Subgroup sp handles samples [sp * SS, (sp + 1) * SS) of the item (sample index
 // l * P + p); its lane `sub` computes the taps of SPL of them and leaves their records in
@@ -339,13 +279,23 @@ fwd_tiled(const __grid_constant__ Params p) {
     long long item;
     int m;
     long long b;
-    if (p.order == nullptr && p.n_items <= 0x7fffffffLL) {
-        // 32-bit index arithmetic (the launch checks the item count)
+    if (p.n_items <= 0x7fffffffLL) {
+        // 32-bit index arithmetic while every item index fits
         const unsigned it = static_cast<unsigned>(pos);
-        const unsigned bq = it / static_cast<unsigned>(p.M);
+        const unsigned bq = it / static_cast<unsigned>(p.M);       // b * Nq + i
         m = static_cast<int>(it - bq * static_cast<unsigned>(p.M));
-        b = bq / static_cast<unsigned>(p.Nq);
-        item = it;
+        const unsigned bb = bq / static_cast<unsigned>(p.Nq);
+        b = bb;
+        if (p.order == nullptr) {
+            item = it;
+        } else {
+            // query order: position i of batch b runs query order[b * Nq + i], clamped into
+            // [0, Nq) (a malformed order gives wrong results, never an out-of-range access)
+            int q = __ldg(p.order + bq);
+            q = q < 0 ? 0 : (q >= p.Nq ? static_cast<int>(p.Nq - 1) : q);
+            item = (static_cast<unsigned>(bb) * static_cast<unsigned>(p.Nq) + q) *
+                       static_cast<unsigned>(p.M) + m;
+        }
     } else {
         item = ordered_item(p, pos);
         m = static_cast<int>(item % p.M);
