@@ -295,6 +295,31 @@ const char *msda_last_error(void);
 /* Version of this interface (major * 10000 + minor * 100 + patch). */
 int32_t msda_abi_version(void);
 
+/*
+ * Bounds-checking build.  The pages fix no such facility; it is a debugging aid of this
+ * library.  The same sources compiled with MSDA_DEBUG_BOUNDS give libmsda_debug.so, with
+ * the same entry points: before every value-row access (loads in the forward and
+ * backward, grad_value reductions in the backward) a kernel checks the corner's row index
+ * against [0, Nin); a row outside that range is skipped, and the first one met on the
+ * device is recorded (with its batch, query, head, level and point; no trap, no wait).
+ * With correct index arithmetic and valid arguments nothing is ever recorded.
+ *
+ * msda_build_flags: MSDA_BUILD_DEBUG_BOUNDS when this library checks, else 0.
+ * msda_debug_bounds_status: debug build: synchronises the current device, reads and
+ *   clears its record, and returns MSDA_ERR_INTERNAL with the offender in
+ *   msda_last_error() when one was recorded since the last call, else MSDA_OK.  Normal
+ *   build: MSDA_OK (nothing is checked); no CUDA call.
+ * msda_debug_bounds_selftest: debug build: enqueues on `stream` one thread that runs the
+ *   kernels' check on a made-up offender (Nin = 10, row -5, batch 1, query 2, head 1,
+ *   level 1, point 1 of Nq = 7, M = 3, P = 2), which the next status call reports; it
+ *   touches no memory but the record.  Normal build: MSDA_ERR_UNSUPPORTED.
+ * Records are per device; calls whose work overlaps on the GPU share the record.
+ */
+#define MSDA_BUILD_DEBUG_BOUNDS 1
+int32_t msda_build_flags(void);
+msda_status msda_debug_bounds_status(void);
+msda_status msda_debug_bounds_selftest(msda_stream_t stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

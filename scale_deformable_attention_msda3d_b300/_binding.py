@@ -28,7 +28,9 @@ EXPORTS = ("msda2d_forward", "msda2d_backward", "msda3d_forward", "msda3d_backwa
            "msda_query_order_workspace_size", "msda2d_forward_ordered", "msda3d_forward_ordered",
            "msda_query_order_static", "msda2d_forward_pruned", "msda3d_forward_pruned",
            "msda2d_forward_fused", "msda3d_forward_fused", "msda2d_backward_fused",
-           "msda3d_backward_fused")
+           "msda3d_backward_fused", "msda_build_flags", "msda_debug_bounds_status",
+           "msda_debug_bounds_selftest")
+MSDA_BUILD_DEBUG_BOUNDS = 1
 
 
 class MsdaError(RuntimeError):
@@ -60,13 +62,16 @@ def library_path() -> str:
 
 
 def load(path: Optional[str] = None):
-    """Load libmsda.so (building it in-tree first when missing or stale)."""
+    """Load libmsda.so (building it in-tree first when missing or stale).  The environment
+    variable MSDA_LIBRARY, when set, names the library the module functions use instead
+    (for example the bounds-checking build, libmsda_debug.so)."""
     global _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
+        default = path is None
         if path is None:
-            path = _builder().build()
+            path = os.environ.get("MSDA_LIBRARY") or _builder().build()
         if not os.path.exists(path):
             raise RuntimeError(f"libmsda not found at {path}")
         lib = ctypes.CDLL(path)
@@ -105,7 +110,13 @@ def load(path: Optional[str] = None):
         lib.msda_last_error.restype = ctypes.c_char_p
         lib.msda_abi_version.argtypes = []
         lib.msda_abi_version.restype = ctypes.c_int32
-        if path == _builder().LIB:
+        lib.msda_build_flags.argtypes = []
+        lib.msda_build_flags.restype = ctypes.c_int32
+        lib.msda_debug_bounds_status.argtypes = []
+        lib.msda_debug_bounds_status.restype = ctypes.c_int
+        lib.msda_debug_bounds_selftest.argtypes = [_VP]
+        lib.msda_debug_bounds_selftest.restype = ctypes.c_int
+        if default or path == _builder().LIB:
             _lib = lib
         return lib
 
@@ -570,6 +581,19 @@ def msda3d_forward_pruned(value, spatial_shapes, level_start_index, sampling_loc
 def msda_last_error() -> str:
     lib = load()
     return lib.msda_last_error().decode(errors="replace")
+
+
+def msda_build_flags() -> int:
+    return int(load().msda_build_flags())
+
+
+def msda_debug_bounds_status() -> int:
+    """Status of the bounds-check record (see include/msda.h); returns the status code."""
+    return int(load().msda_debug_bounds_status())
+
+
+def msda_debug_bounds_selftest(stream: int = 0) -> int:
+    return int(load().msda_debug_bounds_selftest(_VP(stream)))
 
 
 def msda_abi_version() -> int:

@@ -1,10 +1,13 @@
 """Builds libmsda.so in-tree with nvcc for sm_103a (B300).
 
-    python -m scale_deformable_attention_msda3d_b300.build [--force]
+    python -m scale_deformable_attention_msda3d_b300.build [--force] [--debug-bounds]
 
 Objects go to ``_build/`` next to this file; the shared library is written next to this
 file as ``libmsda.so``.  Sources are compiled in parallel, then linked with the static
-CUDA runtime so that loading the library needs no GPU.
+CUDA runtime so that loading the library needs no GPU.  ``--debug-bounds`` (or
+build(debug=True)) compiles the same sources with MSDA_DEBUG_BOUNDS into ``_build_debug/``
+and ``libmsda_debug.so``: every corner row index is checked before its access and the
+first offender recorded (include/msda.h, bounds-checking build).
 """
 from __future__ import annotations
 
@@ -21,6 +24,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmsda.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libmsda_debug.so")
 HEADERS = [os.path.join(ROOT, "include", "msda.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -45,21 +50,27 @@ def _inputs() -> List[str]:
                                   if f.endswith((".cuh", ".h"))] + [os.path.abspath(__file__)]
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB):
+def is_stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: List[str] = ()) -> str:
-    if not force and not is_stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: List[str] = (),
+          debug: bool = False) -> str:
+    """Build libmsda.so (debug=True: libmsda_debug.so with the bounds checks)."""
+    lib_out = LIB_DEBUG if debug else LIB
+    build_dir = BUILD_DEBUG if debug else BUILD
+    if debug:
+        extra_flags = [*extra_flags, "-DMSDA_DEBUG_BOUNDS"]
+    if not force and not is_stale(lib_out):
+        return lib_out
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -72,13 +83,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags: List[str] = (
 
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_out + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_out)
+    return lib_out
 
 
 def main(argv=None) -> int:
@@ -87,10 +98,12 @@ def main(argv=None) -> int:
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--ptxas-info", action="store_true",
                     help="print registers / spills / shared memory per kernel")
+    ap.add_argument("--debug-bounds", action="store_true",
+                    help="build libmsda_debug.so (corner row indices checked before access)")
     a = ap.parse_args(argv)
     extra = ["-Xptxas", "-v"] if a.ptxas_info else []
     print(build(force=a.force or a.ptxas_info, verbose=a.verbose or a.ptxas_info,
-                extra_flags=extra))
+                extra_flags=extra, debug=a.debug_bounds))
     return 0
 
 

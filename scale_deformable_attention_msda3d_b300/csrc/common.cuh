@@ -159,6 +159,35 @@ __device__ __forceinline__ void logit_stats(const float *z, int S, float &mx, fl
     for (int i = 0; i < S; ++i) sum += expf(__ldg(z + i) - mx);
 }
 
+// ------------------------------------------------------------------ debug bounds checks
+
+// row_ok(p, row, item, sample): true when the corner row index lies in [0, N_in).  In a
+// build with MSDA_DEBUG_BOUNDS a row outside that range is recorded in *p.dbg (the first
+// one only: the flag is claimed with atomicCAS, no trap, no wait) and the caller skips the
+// access; in the normal build the function is the constant true and costs nothing.
+__device__ __forceinline__ bool row_ok(const Params &p, long long row, long long item,
+                                       int sample) {
+#ifdef MSDA_DEBUG_BOUNDS
+    if (row >= 0 && row < p.Nin) return true;
+    DebugRecord *d = p.dbg;
+    if (d != nullptr && atomicCAS(&d->flag, 0u, 1u) == 0u) {
+        d->sample = sample;
+        d->row = row;
+        d->item = item;
+        d->nin = p.Nin;
+        d->nq = p.Nq;
+        d->m_count = p.M;
+        d->p_count = p.P;
+        __threadfence();
+        atomicExch(&d->flag, 2u);
+    }
+    return false;
+#else
+    (void)p; (void)row; (void)item; (void)sample;
+    return true;
+#endif
+}
+
 // ------------------------------------------------------------------ per-sample taps
 
 constexpr unsigned kFull = 0xffffffffu;

@@ -175,6 +175,9 @@ msda_status forward_impl(int ndim, const msda_dims *dims, const void *value,
     p.order = ordered ? order : nullptr;
     p.prune = prune;
     p.ref = fused ? ref : nullptr;
+#ifdef MSDA_DEBUG_BOUNDS
+    MSDA_TRY(cuda_status(msda::debug_record(&p.dbg), "bounds-check record"));
+#endif
     return cuda_status(msda::launch_forward(ndim, dims->value_dtype, G, p,
                                             reinterpret_cast<cudaStream_t>(stream)),
                        "forward launch");
@@ -215,6 +218,9 @@ msda_status backward_impl(int ndim, const msda_dims *dims, const void *value,
     p.grad_attn = grad_attn;
     p.ref = fused ? ref : nullptr;
     p.grad_ref = fused ? grad_ref : nullptr;
+#ifdef MSDA_DEBUG_BOUNDS
+    MSDA_TRY(cuda_status(msda::debug_record(&p.dbg), "bounds-check record"));
+#endif
     return cuda_status(msda::launch_backward(ndim, dims->value_dtype, G, p, s),
                        fused ? "fused backward launch" : "backward launch");
 }
@@ -427,6 +433,53 @@ msda_status msda3d_backward_fused(const msda_dims *dims, const void *value,
                          attention_logits, grad_out, grad_value, grad_sampling_offsets,
                          grad_attention_logits, stream, reference_points, grad_reference_points,
                          true);
+}
+
+int32_t msda_build_flags(void) {
+#ifdef MSDA_DEBUG_BOUNDS
+    return MSDA_BUILD_DEBUG_BOUNDS;
+#else
+    return 0;
+#endif
+}
+
+msda_status msda_debug_bounds_status(void) {
+#ifdef MSDA_DEBUG_BOUNDS
+    msda::DebugRecord r;
+    MSDA_TRY(cuda_status(msda::debug_record_take(&r), "reading the bounds-check record"));
+    if (r.flag == 0) return MSDA_OK;
+    const long long M = r.m_count > 0 ? r.m_count : 1, P = r.p_count > 0 ? r.p_count : 1;
+    const long long Nq = r.nq > 0 ? r.nq : 1;
+    const long long bq = r.item / M;
+    return fail(MSDA_ERR_INTERNAL,
+                "bounds check: corner row %lld outside [0, %lld) at batch %lld, query %lld, "
+                "head %lld, level %lld, point %lld",
+                r.row, r.nin, bq / Nq, bq % Nq, r.item % M, (long long)r.sample / P,
+                (long long)r.sample % P);
+#else
+    return MSDA_OK;
+#endif
+}
+
+msda_status msda_debug_bounds_selftest(msda_stream_t stream) {
+#ifdef MSDA_DEBUG_BOUNDS
+    // a made-up offender: N_in = 10, Nq = 7, M = 3, P = 2; row -5 at item (b=1, q=2, m=1),
+    // sample (l=1, p=1); the check records it and nothing is accessed
+    msda::Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.Nin = 10;
+    p.Nq = 7;
+    p.M = 3;
+    p.P = 2;
+    MSDA_TRY(cuda_status(msda::debug_record(&p.dbg), "bounds-check record"));
+    return cuda_status(msda::launch_debug_selftest(p, -5, (1 * 7 + 2) * 3 + 1, 1 * 2 + 1,
+                                                   reinterpret_cast<cudaStream_t>(stream)),
+                       "bounds-check self-test launch");
+#else
+    (void)stream;
+    return fail(MSDA_ERR_UNSUPPORTED,
+                "bounds checks are compiled only into the debug build (MSDA_DEBUG_BOUNDS)");
+#endif
 }
 
 const char *msda_last_error(void) { return g_err; }

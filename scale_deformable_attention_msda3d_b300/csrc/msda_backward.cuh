@@ -107,8 +107,13 @@ bwd2d_generic(const __grid_constant__ Params p) {
             const bool ok = okx && oky;
             const bool vx0 = ok && x0 >= 0, vx1 = ok && x0 < W - 1;
             const bool vy0 = y0 >= 0, vy1 = y0 < H - 1;
-            const bool ok00 = vy0 && vx0, ok01 = vy0 && vx1, ok10 = vy1 && vx0, ok11 = vy1 && vx1;
             const long long r00 = static_cast<long long>(y0 * W + x0);
+            const long long a00 = p.start[l] + r00;  // row index within the batch
+            const int sidx = l * P + k;
+            const bool ok00 = vy0 && vx0 && row_ok(p, a00, item, sidx);
+            const bool ok01 = vy0 && vx1 && row_ok(p, a00 + 1, item, sidx);
+            const bool ok10 = vy1 && vx0 && row_ok(p, a00 + W, item, sidx);
+            const bool ok11 = vy1 && vx1 && row_ok(p, a00 + W + 1, item, sidx);
             const char *c00 = vl + r00 * rb;
             uint4 u00 = make_uint4(0, 0, 0, 0), u01 = u00, u10 = u00, u11 = u00;
             if (ok00) u00 = ldg16(c00);
@@ -206,9 +211,10 @@ bwd3d_generic(const __grid_constant__ Params p) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
-                ok[c] = vx[dx] && vy[dy] && vz[dz];
-                any = any || ok[c];
                 off[c] = dz * HW + dy * W + dx;
+                ok[c] = vx[dx] && vy[dy] && vz[dz] &&
+                        row_ok(p, p.start[l] + r000 + off[c], item, static_cast<int>(l * P + k));
+                any = any || ok[c];
                 uint4 u = make_uint4(0, 0, 0, 0);
                 if (ok[c]) u = ldg16(c000 + off[c] * rb);
                 d[c] = dot(u, g);
@@ -414,7 +420,11 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
-                    const bool in = (ok >> c) & 1u;
+                    const bool in =
+                        ((ok >> c) & 1u) &&
+                        row_ok(p, static_cast<long long>(row) + dx + (dy ? p.W[l] : 0) +
+                                      (dz ? static_cast<long long>(p.W[l]) * p.H[l] : 0),
+                               item, s);
                     const char *src = cy[dy] + (dz ? p.sz[l] : 0) + (dx ? rb : 0);
                     Slice<16> u;
                     load_slice_if(in, src, u);

@@ -82,17 +82,23 @@ fwd2d_generic(const __grid_constant__ Params p) {
             const bool ok = okx && oky && !(fabsf(a) < p.prune);
             const bool vx0 = ok && x0 >= 0, vx1 = ok && x0 < W - 1;
             const bool vy0 = y0 >= 0, vy1 = y0 < H - 1;
+            const long long r00 = p.start[l] + static_cast<long long>(y0) * W + x0;
+            const int sidx = l * P + k;
+            const bool k00 = vy0 && vx0 && row_ok(p, r00, item, sidx);
+            const bool k01 = vy0 && vx1 && row_ok(p, r00 + 1, item, sidx);
+            const bool k10 = vy1 && vx0 && row_ok(p, r00 + W, item, sidx);
+            const bool k11 = vy1 && vx1 && row_ok(p, r00 + W + 1, item, sidx);
             const float ay0 = a * (1.f - fy), ay1 = a * fy;
-            const float w00 = (vy0 && vx0) ? ay0 * (1.f - fx) : 0.f;
-            const float w01 = (vy0 && vx1) ? ay0 * fx : 0.f;
-            const float w10 = (vy1 && vx0) ? ay1 * (1.f - fx) : 0.f;
-            const float w11 = (vy1 && vx1) ? ay1 * fx : 0.f;
+            const float w00 = k00 ? ay0 * (1.f - fx) : 0.f;
+            const float w01 = k01 ? ay0 * fx : 0.f;
+            const float w10 = k10 ? ay1 * (1.f - fx) : 0.f;
+            const float w11 = k11 ? ay1 * fx : 0.f;
             const char *c00 = vl + static_cast<long long>(y0 * W + x0) * rb;
             uint4 u00 = make_uint4(0, 0, 0, 0), u01 = u00, u10 = u00, u11 = u00;
-            if (vy0 && vx0) u00 = ldg16(c00);
-            if (vy0 && vx1) u01 = ldg16(c00 + rb);
-            if (vy1 && vx0) u10 = ldg16(c00 + W * rb);
-            if (vy1 && vx1) u11 = ldg16(c00 + (W + 1) * rb);
+            if (k00) u00 = ldg16(c00);
+            if (k01) u01 = ldg16(c00 + rb);
+            if (k10) u10 = ldg16(c00 + W * rb);
+            if (k11) u11 = ldg16(c00 + (W + 1) * rb);
             float v[N];
             unpack(u00, v);
 #pragma unroll
@@ -170,7 +176,10 @@ fwd3d_generic(const __grid_constant__ Params p) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
-                const bool inside = vx[dx] && vy[dy] && vz[dz];
+                const bool inside =
+                    vx[dx] && vy[dy] && vz[dz] &&
+                    row_ok(p, p.start[l] + (static_cast<long long>(z0 + dz) * H + (y0 + dy)) * W +
+                                  x0 + dx, item, l * P + k);
                 w[c] = inside ? wz[dz] * wy[dy] * wx[dx] : 0.f;
                 u[c] = make_uint4(0, 0, 0, 0);
                 if (inside) u[c] = ldg16(c000 + dz * sz + dy * sy + dx * rb);
@@ -401,7 +410,16 @@ fwd_tiled(const __grid_constant__ Params p) {
         for (int c = 0; c < NC; ++c) {
             const char *base = cy[(c >> 1) & 1];
             if (c >> 2) base += p.sz[l];
-            const bool in = (tq[slot].ok >> c) & 1u;
+            bool in = (tq[slot].ok >> c) & 1u;
+#ifdef MSDA_DEBUG_BOUNDS
+            const long long crow = static_cast<long long>(tq[slot].row) + (c & 1) +
+                                   (((c >> 1) & 1) ? p.W[l] : 0) +
+                                   ((c >> 2) ? static_cast<long long>(p.W[l]) * p.H[l] : 0);
+            if (in && !row_ok(p, crow, item, s0 + s)) {
+                in = false;
+                tq[slot].ok &= ~(1u << c);
+            }
+#endif
             if constexpr (PRED) {
                 load_slice_if(in, base + ((c & 1) ? rb : 0), u[slot][c]);
             } else {

@@ -11,6 +11,19 @@ constexpr int kBF16 = 1;
 constexpr int kMaxLevels = 16;
 constexpr int kMaxPoints = 32;
 
+// First out-of-range corner row seen by a kernel of a build with MSDA_DEBUG_BOUNDS (the
+// debug build checks every corner row index against [0, N_in) before its access, records
+// the first offender here and skips the access).  flag: 0 none, 1 being written, 2 set.
+struct DebugRecord {
+    unsigned flag;
+    int sample;        // l * P + p
+    long long row;     // the offending row index within its batch
+    long long item;    // (b * Nq + q) * M + m
+    long long nin;     // N_in, Nq, M and P of the call, to decode item and sample
+    long long nq;
+    int m_count, p_count;
+};
+
 // Everything a kernel needs, passed by value as a __grid_constant__ parameter.
 // All level geometry is validated on the host before it gets here.
 struct Params {
@@ -44,6 +57,7 @@ struct Params {
     float fW[kMaxLevels], fH[kMaxLevels], fZ[kMaxLevels];
     long long sy[kMaxLevels];   // bytes between value rows one image row apart (W * row_bytes)
     long long sz[kMaxLevels];   // bytes between value rows one slice apart (H * W * row_bytes)
+    DebugRecord *dbg;           // debug build: where a kernel records an out-of-range row
     // backward work split: CTA c handles batch b = c / (M * nchunk), head m = (c / nchunk) % M,
     // and queries [chunk * qchunk, (chunk + 1) * qchunk) with chunk = c % nchunk
     int nchunk, qchunk;
@@ -82,6 +96,15 @@ cudaError_t launch_query_order(int ndim, const Params &p, int *order, int *hist,
 // The same order with its scratch in a fixed device array of the library
 // (msda_order_static.cu); static_order_fits tells whether (B, Nq) fits that array.
 bool static_order_fits(long long B, long long Nq);
+
+// Debug build (MSDA_DEBUG_BOUNDS, msda_debug.cu): the device address of this device's
+// DebugRecord (looked up once per device), reading and clearing it, and a kernel that
+// records a made-up offender so that the reporting path can be tested without any
+// out-of-range access.  Without MSDA_DEBUG_BOUNDS these return cudaErrorNotSupported.
+cudaError_t debug_record(DebugRecord **ptr);
+cudaError_t debug_record_take(DebugRecord *out);
+cudaError_t launch_debug_selftest(const Params &p, long long row, long long item, int sample,
+                                  cudaStream_t stream);
 cudaError_t launch_query_order_static(int ndim, const Params &p, int *order, cudaStream_t stream);
 
 }  // namespace msda

@@ -345,3 +345,36 @@ def test_query_order_grid_too_large_is_a_cuda_error_with_nothing_enqueued(lib):
     st = msda.query_order_raw(2, d, FAKE, FAKE, FAKE, need, 0)
     assert st == msda.MSDA_ERR_CUDA, msda.msda_last_error()
     assert "cudaErrorInvalidConfiguration" in msda.msda_last_error()
+
+
+def test_normal_build_has_no_bounds_checks(lib):
+    """libmsda.so reports no checks, its status call is a no-op and its self-test is
+    unsupported (all without a CUDA call)."""
+    assert msda.msda_build_flags() == 0
+    assert msda.msda_debug_bounds_status() == msda.MSDA_OK
+    assert msda.msda_debug_bounds_selftest(0) == msda.MSDA_ERR_UNSUPPORTED
+    assert "debug build" in msda.msda_last_error()
+
+
+def test_debug_build_loads_and_exports_every_symbol():
+    """libmsda_debug.so (MSDA_DEBUG_BOUNDS) exports the same entry points and says so in
+    its build flags; without a device its status call fails as a CUDA error."""
+    import json
+    import subprocess
+    import sys
+    from scale_deformable_attention_msda3d_b300 import build
+    path = build.build(debug=True)
+    raw = ctypes.CDLL(path)
+    for name in declared_functions():
+        getattr(raw, name)
+    script = ("import json, sys; sys.path.insert(0, sys.argv[1]); "
+              "import scale_deformable_attention_msda3d_b300 as m; m.load(); "
+              "print(json.dumps([m.msda_build_flags(), m.msda_debug_bounds_status(), "
+              "m.msda_last_error()]))")
+    env = dict(os.environ, MSDA_LIBRARY=path, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", script, ROOT], env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    flags, st, msg = json.loads(r.stdout.strip().splitlines()[-1])
+    assert flags == msda.MSDA_BUILD_DEBUG_BOUNDS
+    assert st == msda.MSDA_ERR_CUDA and "bounds-check record" in msg
