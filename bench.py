@@ -929,6 +929,89 @@ def run_reference(args):
             "gpu_launches": 0}
 
 
+# ----------------------------------------------------------------------------- probes
+
+PROBES = (
+    # name, kind, rows in the buffer (128 bytes each), lanes per row, what it measures
+    ("gather16_l1", 0, 256, 8, "random 128-B rows, 16-B lanes, 32 KB buffer (L1-resident)"),
+    ("gather16_l2", 0, 320_000, 8, "random 128-B rows, 16-B lanes, 41 MB buffer (L2-resident)"),
+    ("gather16_hbm", 0, 1 << 24, 8, "random 128-B rows, 16-B lanes, 2.1 GB buffer (HBM)"),
+    ("gather32_l1", 1, 256, 4, "random 128-B rows, 32-B lanes, 32 KB buffer (L1-resident)"),
+    ("gather32_l2", 1, 320_000, 4, "random 128-B rows, 32-B lanes, 41 MB buffer (L2-resident)"),
+    ("gather32_hbm", 1, 1 << 24, 4, "random 128-B rows, 32-B lanes, 2.1 GB buffer (HBM)"),
+    ("reduce_l2", 2, 320_000, 8, "red.global.add.v4.f32 of random 128-B rows of a 41 MB buffer"),
+    ("reduce_hot247", 2, 247, 8, "red.global.add.v4.f32 of random rows of a 247-row hot set"),
+    ("smem_atomic_247", 3, 0, 8, "per-channel shared-memory fp32 atomics into a 247-row tile"),
+    ("smem_owner_247", 4, 0, 8, "owner-computes shared-memory row updates (no atomics), "
+                                "247-row tile"),
+    ("tma_gather_l2", 5, 320_000, 1, "cp.async.bulk of random 128-B rows into shared memory, "
+                                     "41 MB buffer"),
+)
+
+
+def run_probes(args):
+    """The on-chip rates the kernels are bound by, measured by libmsda_probes.so: random
+    128-byte row gathers, reductions and shared-memory updates; rows per second and rows
+    per SM clock.  Prints one JSON line per probe."""
+    import ctypes
+    import torch
+    from scale_deformable_attention_msda3d_b300 import build
+    lib = ctypes.CDLL(build.build_probes())
+    lib.msda_probe_launch.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_uint, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_uint, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p]
+    lib.msda_probe_launch.restype = ctypes.c_int
+    lib.msda_probe_block.argtypes = [ctypes.c_int]
+    dev = torch.device("cuda", 0)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    stream = torch.cuda.Stream(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for name, kind, n_rows, lanes, what in PROBES:
+        if args.probe not in ("all", name):
+            continue
+        threads = lib.msda_probe_block(kind)
+        blocks = sms * (2048 // threads)
+        buf = torch.zeros(max(n_rows, 1) * 32, dtype=torch.float32, device=dev)
+        if kind in (0, 1, 5):
+            buf.uniform_()
+        sink = torch.empty(blocks * threads, dtype=torch.float32, device=dev)
+        iters = 256 if kind != 5 else 64
+        rows_per_launch = blocks * threads // lanes * iters if kind != 5 else blocks * threads * iters
+
+        def launch(seed):
+            rc = lib.msda_probe_launch(kind, ctypes.c_void_p(buf.data_ptr()), n_rows, blocks, iters,
+                                       seed, ctypes.c_void_p(sink.data_ptr()),
+                                       ctypes.c_void_p(err.data_ptr()),
+                                       ctypes.c_void_p(stream.cuda_stream))
+            if rc != 0:
+                raise RuntimeError(f"probe {name}: launch status {rc}")
+
+        for i in range(3):
+            launch(i)
+        torch.cuda.synchronize(dev)
+        times = []
+        for r in range(5):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch(100 + r)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1) / 1e3)
+        if int(err.item()) != 0:
+            raise RuntimeError(f"probe {name}: a bounded wait ran out")
+        t = statistics.median(times)
+        rate = rows_per_launch / t
+        line = {"probe": name, "what": what, "rows_per_s": rate, "row_bytes": 128,
+                "bytes_per_s": rate * 128, "rows_per_launch": rows_per_launch,
+                "launch_us": t * 1e6, "blocks": blocks, "threads": threads, "sms": sms,
+                "rows_per_sm_clock_at_2032mhz": rate / (sms * 2.032e9)}
+        print(json.dumps(line), flush=True)
+        del buf, sink
+    return None
+
+
 def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -960,6 +1043,9 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline leg")
+    ap.add_argument("--probe", default=None,
+                    help="run the on-chip rate microbenchmarks instead of the step ('all' or "
+                         "one probe name) and print one JSON line per probe")
     return ap
 
 
@@ -974,6 +1060,9 @@ def main(argv=None):
         ap.error("--order, --prune and --fused are separate modes")
     if args.fused:
         args.no_e2e = True
+    if args.probe:
+        run_probes(args)
+        return 0
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)

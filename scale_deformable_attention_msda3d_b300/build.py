@@ -26,6 +26,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmsda.so")
 BUILD_DEBUG = os.path.join(PKG, "_build_debug")
 LIB_DEBUG = os.path.join(PKG, "libmsda_debug.so")
+PROBES_SRC = os.path.join(CSRC, "probes", "msda_probes.cu")
+LIB_PROBES = os.path.join(PKG, "libmsda_probes.so")
 HEADERS = [os.path.join(ROOT, "include", "msda.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -90,6 +92,22 @@ def build(force: bool = False, verbose: bool = False, extra_flags: List[str] = (
         raise RuntimeError(f"link failed:\n{r.stdout}{r.stderr}")
     os.replace(tmp, lib_out)
     return lib_out
+
+
+def build_probes(force: bool = False) -> str:
+    """Build libmsda_probes.so, the on-chip rate microbenchmarks that bench.py --probe runs
+    (not part of libmsda)."""
+    if (not force and os.path.exists(LIB_PROBES)
+            and os.path.getmtime(LIB_PROBES) >= os.path.getmtime(PROBES_SRC)):
+        return LIB_PROBES
+    tmp = LIB_PROBES + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+           "-cudart", "static", "-o", tmp, PROBES_SRC]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on msda_probes.cu:\n{r.stdout}{r.stderr}")
+    os.replace(tmp, LIB_PROBES)
+    return LIB_PROBES
 
 
 def main(argv=None) -> int:
