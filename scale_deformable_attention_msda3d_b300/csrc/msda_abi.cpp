@@ -111,6 +111,7 @@ msda_status build_params(const msda_dims *d, int ndim, const int64_t *shapes,
     p->n_items = items;
     p->row_bytes = int64_t(d->M) * dbytes;
     p->rb32 = int(p->row_bytes);
+    p->pinv = int((65536 + d->P - 1) / d->P);
     // the forward's tap records may carry the corner-validity bits under the row of corner
     // 0 (4 bits in 2D, 8 in 3D) while that row, in [-(H*W + W + 1), N_in), fits the rest
     p->pack_taps = d->Nin < (int64_t(1) << (ndim == 2 ? 27 : 22)) ? 1 : 0;

@@ -30,6 +30,8 @@
 // * fwd{2,3}d_generic (any L, P): every lane of the group computes every sample itself.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace msda {
@@ -254,25 +256,35 @@ template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 1, MI
 // l * P + p); its lane `sub` computes the taps of SPL of them and leaves their records in
 // shared memory.  The group then walks its samples: the corner rows of the next AHEAD
 // samples are loaded (in-level corners only) before the current sample is summed.
+//
+// LL = 0 selects the runtime-(L, P) form: L and P come from the parameters, PP is the
+// largest L * P it handles (SMAX), and the sample walk is a loop unrolled by DEPTH instead
+// of a fully unrolled sequence; the level of sample j is (j * p.pinv) >> 16.
 template <int DT, int G, int VB, int NDIM, int LL, int PP, int SPLIT, int AHEAD, int MINB,
           bool FUSED, bool PACK, bool PRED>
 __global__ void __launch_bounds__(kFwdBlock, MINB)
 fwd_tiled(const __grid_constant__ Params p) {
+    constexpr bool RT = LL == 0;
     constexpr int N = VB / Vec<DT>::ESIZE;  // channels per lane
     constexpr int NC = 1 << NDIM;
-    constexpr int S = LL * PP;
-    static_assert(S % SPLIT == 0, "SPLIT must divide L * P");
-    constexpr int SS = S / SPLIT;
-    constexpr int SPL = (SS + G - 1) / G;
+    constexpr int SMAX = RT ? PP : LL * PP;           // samples per item (at most, if RT)
+    static_assert(RT || SMAX % SPLIT == 0, "SPLIT must divide L * P");
+    constexpr int SPLM = ((SMAX + SPLIT - 1) / SPLIT + G - 1) / G;  // taps per lane (at most)
     constexpr int LANES = G * SPLIT;
     static_assert(LANES <= 32 && (32 % LANES) == 0, "lanes per item must divide the warp");
-    // when every lane owns exactly SPL samples, read them with vector loads
-    constexpr bool EVEN = (SS % G) == 0;
-    constexpr int ALOC = cmin(cmin(falign(S * NDIM), falign(SS * NDIM)), falign(SPL * NDIM));
-    constexpr int AATT = cmin(cmin(falign(S), falign(SS)), falign(SPL));
+    // compiled (L, P): when every lane owns exactly SPL samples, read them with vector loads
+    constexpr int SSC = SMAX / SPLIT;
+    constexpr bool EVEN = !RT && (SSC % G) == 0;
+    constexpr int ALOC = cmin(cmin(falign(SMAX * NDIM), falign(SSC * NDIM)), falign(SPLM * NDIM));
+    constexpr int AATT = cmin(cmin(falign(SMAX), falign(SSC)), falign(SPLM));
     constexpr int DEPTH = AHEAD + 1;
     constexpr int IPB = kFwdBlock / LANES;            // items per block
-    constexpr int ISTR = tap_slot(S - 1) + 2;         // slots per item (+1 pad between items)
+    constexpr int ISTR = tap_slot(SMAX - 1) + 2;      // slots per item (+1 pad between items)
+    const int S = RT ? p.L * p.P : SMAX;              // samples per item
+    const int SS = S / SPLIT;                         // samples per subgroup
+    const int SPL = RT ? (SS + G - 1) / G : SPLM;     // taps per lane
+    // level of sample j
+    auto level = [&](int j) { return RT ? (j * p.pinv) >> 16 : j / PP; };
     constexpr int OKB = NDIM == 2 ? 4 : 8;            // validity bits under a packed row
 
     __shared__ float4 rec[IPB * ISTR];
@@ -318,54 +330,56 @@ fwd_tiled(const __grid_constant__ Params p) {
     const int my0 = s0 + sub * SPL;          // first sample whose taps this lane computes
 
     // 1. locations and weights of this lane's samples, then their tap records
-    float lv[SPL * NDIM], av[SPL];
+    float lv[SPLM * NDIM], av[SPLM];
     const float *lsrc = p.loc + (item * S + my0) * NDIM;
     const float *asrc = p.attn + item * S + my0;
+    // sample my0 + i is this lane's and exists
+    auto have = [&](int i) { return EVEN || ((!RT || i < SPL) && sub * SPL + i < SS); };
     if constexpr (EVEN) {
-        load_stream<SPL * NDIM, ALOC>(lsrc, lv);
-        load_stream<SPL, AATT>(asrc, av);
+        load_stream<SPLM * NDIM, ALOC>(lsrc, lv);
+        load_stream<SPLM, AATT>(asrc, av);
     } else {
 #pragma unroll
-        for (int i = 0; i < SPL; ++i) {
-            const bool have = sub * SPL + i < SS;
+        for (int i = 0; i < SPLM; ++i) {
+            const bool h = have(i);
 #pragma unroll
-            for (int k = 0; k < NDIM; ++k) lv[i * NDIM + k] = have ? __ldcs(lsrc + i * NDIM + k) : 0.f;
-            av[i] = have ? __ldcs(asrc + i) : 0.f;
+            for (int k = 0; k < NDIM; ++k) lv[i * NDIM + k] = h ? __ldcs(lsrc + i * NDIM + k) : 0.f;
+            av[i] = h ? __ldcs(asrc + i) : 0.f;
         }
     }
     if constexpr (FUSED) {
         // prologue: softmax of the item's logits over all its lanes, then the locations
         float mx = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < SPL; ++i)
-            if (EVEN || sub * SPL + i < SS) mx = fmaxf(mx, av[i]);
+        for (int i = 0; i < SPLM; ++i)
+            if (have(i)) mx = fmaxf(mx, av[i]);
 #pragma unroll
         for (int o = 1; o < LANES; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
         float sum = 0.f;
 #pragma unroll
-        for (int i = 0; i < SPL; ++i) {
-            av[i] = (EVEN || sub * SPL + i < SS) ? expf(av[i] - mx) : 0.f;
+        for (int i = 0; i < SPLM; ++i) {
+            av[i] = have(i) ? expf(av[i] - mx) : 0.f;
             sum += av[i];
         }
 #pragma unroll
         for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(kFull, sum, o);
         const long long bq = item / p.M;
 #pragma unroll
-        for (int i = 0; i < SPL; ++i) {
+        for (int i = 0; i < SPLM; ++i) {
             av[i] = __fdiv_rn(av[i], sum);
-            const int l = cmin(my0 + i, s0 + SS - 1) / PP;
+            const int l = level(min(my0 + i, s0 + SS - 1));
 #pragma unroll
             for (int k = 0; k < NDIM; ++k)
                 lv[i * NDIM + k] = fused_location<NDIM>(p, bq, l, k, lv[i * NDIM + k]);
         }
     }
 #pragma unroll
-    for (int i = 0; i < SPL; ++i) {
-        if (!EVEN && sub * SPL + i >= SS) continue;   // past the subgroup's samples
+    for (int i = 0; i < SPLM; ++i) {
+        if (!have(i)) continue;   // past the subgroup's samples
         const int j = my0 + i;
         Taps<NC> tp;
         float fr[NDIM];
-        make_taps(p, j / PP, lv + i * NDIM, av[i], tp, fr);
+        make_taps(p, level(j), lv + i * NDIM, av[i], tp, fr);
         const int slot = ib * ISTR + tap_slot(j);
         const int rbits = PACK ? static_cast<int>((static_cast<unsigned>(tp.row) << OKB) | tp.ok)
                                : tp.row;
@@ -403,7 +417,7 @@ fwd_tiled(const __grid_constant__ Params p) {
 #pragma unroll
             for (int c = 0; c < NC; ++c) tq[slot].w[c] = ((tq[slot].ok >> c) & 1u) ? tq[slot].w[c] : 0.f;
         }
-        const int l = (s0 + s) / PP;  // a constant when SPLIT == 1
+        const int l = level(s0 + s);  // a constant when SPLIT == 1 and (L, P) is compiled
         const char *c0 = vb + static_cast<long long>(tq[slot].row) * p.rb32;
         const char *cy[2] = {c0, c0 + p.sy[l]};
 #pragma unroll
@@ -431,13 +445,25 @@ fwd_tiled(const __grid_constant__ Params p) {
 #pragma unroll
     for (int k = 0; k < AHEAD; ++k)
         if (k < SS) fetch(k, k);
-#pragma unroll
-    for (int s = 0; s < SS; ++s) {
-        if (s + AHEAD < SS) fetch(s + AHEAD, (s + AHEAD) % DEPTH);
-        const int slot = s % DEPTH;
+    // sample s sits in slot s % DEPTH; the loads of sample s + AHEAD are issued before s is
+    // summed.  Compiled (L, P): fully unrolled; runtime (L, P): a loop unrolled by DEPTH, so
+    // that every slot index stays a compile-time constant.
+    auto step = [&](int s, int k) {
+        if (s + AHEAD < SS) fetch(s + AHEAD, (k + AHEAD) % DEPTH);
 #pragma unroll
         for (int c = 0; c < NC; ++c)
-            if (!PRED || ((tq[slot].ok >> c) & 1u)) fma_slice<DT, VB>(acc, tq[slot].w[c], u[slot][c]);
+            if (!PRED || ((tq[k].ok >> c) & 1u)) fma_slice<DT, VB>(acc, tq[k].w[c], u[k][c]);
+    };
+    if constexpr (!RT) {
+#pragma unroll
+        for (int s = 0; s < SSC; ++s) step(s, s % DEPTH);
+    } else {
+#pragma unroll 1
+        for (int sw = 0; sw < SS; sw += DEPTH) {
+#pragma unroll
+            for (int k = 0; k < DEPTH; ++k)
+                if (sw + k < SS) step(sw + k, k);
+        }
     }
 
     // 3. add the subgroups' partial sums, store the item's channels
@@ -472,9 +498,18 @@ int pick_split(long long n_items) {
     return split;
 }
 
+// The runtime-(L, P) form keeps its whole prefetch pipeline live across the loop's back
+// edge, so it takes a shallower window and more registers per thread than the fully
+// unrolled compiled form.
+template <int NDIM, int DT> struct RtShape;
+template <> struct RtShape<2, kF32> { static constexpr int VB = 16, AHEAD = 1, MINB = 8; static constexpr bool PRED = true; };
+template <> struct RtShape<2, kBF16> { static constexpr int VB = 16, AHEAD = 1, MINB = 8; static constexpr bool PRED = false; };
+template <> struct RtShape<3, kF32> { static constexpr int VB = 32, AHEAD = 0, MINB = 5; static constexpr bool PRED = false; };
+template <> struct RtShape<3, kBF16> { static constexpr int VB = 32, AHEAD = 0, MINB = 5; static constexpr bool PRED = false; };
+
 template <int DT, int G, int NDIM, int LL, int PP, int SPLIT>
 cudaError_t launch_tiled(const Params &p, cudaStream_t s) {
-    using SH = Shape<NDIM, DT>;
+    using SH = typename std::conditional<LL == 0, RtShape<NDIM, DT>, Shape<NDIM, DT>>::type;
     const long long threads = p.n_items * G * SPLIT;
     const long long blocks = (threads + kFwdBlock - 1) / kFwdBlock;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -513,11 +548,43 @@ cudaError_t launch_tiled_split(const Params &p, cudaStream_t s) {
     return launch_tiled<DT, G, NDIM, LL, PP, 1>(p, s);
 }
 
+// Runtime-(L, P) form of the compiled path: any L * P up to kRtMaxSamples, for rows of
+// 2 to 16 sixteen-byte lanes.  The split follows pick_split with the runtime sample count.
+constexpr int kRtMaxSamples = 32;
+
+template <int G, int NDIM>
+int pick_split_rt(int S, long long n_items) {
+    constexpr int MAX_SPL = NDIM == 2 ? 4 : 2;
+    constexpr long long kWantThreads = 148LL * 2048 * 2;
+    auto can_double = [S](int split) { return split < 4 && G * split * 2 <= 32 && S % (split * 2) == 0; };
+    int split = 1;
+    while (can_double(split) && S / split > MAX_SPL * G) split *= 2;
+    while (can_double(split) && n_items * G * split < kWantThreads) split *= 2;
+    return split;
+}
+
+template <int DT, int G16, int NDIM>
+cudaError_t launch_tiled_rt(const Params &p, cudaStream_t s) {
+    constexpr int VB = Shape<NDIM, DT>::VB;
+    constexpr int G = G16 * 16 / VB;
+    const int split = pick_split_rt<G, NDIM>(p.L * p.P, p.n_items);
+    if constexpr (G <= 16) {
+        if (split == 2) return launch_tiled<DT, G, NDIM, 0, kRtMaxSamples, 2>(p, s);
+    }
+    if constexpr (G <= 8) {
+        if (split == 4) return launch_tiled<DT, G, NDIM, 0, kRtMaxSamples, 4>(p, s);
+    }
+    return launch_tiled<DT, G, NDIM, 0, kRtMaxSamples, 1>(p, s);
+}
+
 template <int DT, int G, int NDIM>
 cudaError_t forward_nd(const Params &p, cudaStream_t s) {
     if constexpr (G * 16 >= Shape<NDIM, DT>::VB) {
         if (p.L == 4 && p.P == 4) return launch_tiled_split<DT, G, NDIM, 4, 4>(p, s);
         if (p.L == 1 && p.P == 4) return launch_tiled_split<DT, G, NDIM, 1, 4>(p, s);
+    }
+    if constexpr (G >= 2 && G <= 16 && G * 16 >= Shape<NDIM, DT>::VB) {
+        if (p.L * p.P <= kRtMaxSamples) return launch_tiled_rt<DT, G, NDIM>(p, s);
     }
     const long long threads = p.n_items * G;
     const long long blocks = (threads + 255) / 256;

@@ -50,6 +50,7 @@ struct Params {
     int M, D, L, P;
     long long row_bytes;        // M * D * sizeof(value dtype): stride between value rows
     int rb32;                   // row_bytes as a 32-bit int (validated to fit)
+    int pinv;                   // ceil(2^16 / P): level of sample j < 512 is (j * pinv) >> 16
     int pack_taps;              // forward tap records may carry the validity bits under the
                                 // row (N_in < 2^27 in 2D, < 2^22 in 3D)
     // level geometry (entries >= L unused)

@@ -333,3 +333,28 @@ def test_autograd_wrapper_3d_bf16(msda):
     check(host(v.grad), rgv, "bf16", "autograd 3d grad_value", grad_value_magnitude(3, inp))
     check(host(loc.grad), rgl, "f32", "autograd 3d grad_loc")
     check(host(a.grad), rga, "f32", "autograd 3d grad_attn")
+
+
+# ------------------------------------------------------------------ runtime (L, P) path
+
+# (L, P) pairs outside the compiled (4, 4) / (1, 4) with L * P <= 32 take the runtime-(L, P)
+# form of the tiled forward (rows of 2 to 16 sixteen-byte lanes): every sample count from 2
+# to 32 that the pairs below give, narrow and wide rows, a ragged item count, 2D and 3D.
+RT_CASES = [
+    # nd, dtype, D, L, P
+    (2, "f32", 32, 2, 3), (2, "f32", 32, 3, 5), (2, "f32", 32, 5, 4), (2, "f32", 32, 4, 8),
+    (2, "f32", 32, 8, 4), (2, "f32", 32, 2, 16), (2, "f32", 32, 16, 2), (2, "f32", 32, 3, 1),
+    (2, "f32", 16, 4, 2), (2, "f32", 8, 1, 8), (2, "f32", 64, 7, 3),
+    (2, "bf16", 32, 4, 8), (2, "bf16", 32, 3, 4), (2, "bf16", 64, 2, 5), (2, "bf16", 16, 5, 6),
+    (3, "bf16", 32, 4, 8), (3, "bf16", 32, 3, 3), (3, "f32", 16, 2, 4), (3, "f32", 32, 5, 2),
+]
+
+
+@pytest.mark.parametrize("case", RT_CASES, ids=[f"{c[0]}d-{c[1]}-D{c[2]}-L{c[3]}-P{c[4]}"
+                                                for c in RT_CASES])
+def test_runtime_level_point_forward(msda, case):
+    nd, dtype, D, L, P = case
+    inp = workloads.random_problem(nd, _shapes_for(nd, L), B=2, Nq=203, M=3, D=D, P=P,
+                                   dtype=dtype, seed=zlib.crc32(repr(case).encode()),
+                                   backward=False)
+    check_forward(msda, nd, inp, dtype, f"runtime (L, P) fwd {case}")
