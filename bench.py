@@ -58,7 +58,9 @@ KERNEL_SRC_DIR = os.path.join(ROOT, "scale_deformable_attention_msda3d_b300", "c
 KERNEL_FILES = {
     "forward": ("common.cuh", "msda_internal.h", "msda_abi.cpp", "msda_forward.cuh",
                 "msda_forward.cu", "msda_forward_f32_2d.cu", "msda_forward_f32_3d.cu",
-                "msda_forward_bf16_2d.cu", "msda_forward_bf16_3d.cu"),
+                "msda_forward_bf16_2d.cu", "msda_forward_bf16_3d.cu", "msda_forward_rt_f32_2d.cu",
+                "msda_forward_rt_f32_3d.cu", "msda_forward_rt_bf16_2d.cu",
+                "msda_forward_rt_bf16_3d.cu"),
     "backward": ("common.cuh", "msda_internal.h", "msda_abi.cpp", "msda_backward.cuh",
                  "msda_backward.cu", "msda_backward_2d.cu", "msda_backward_3d.cu",
                  "msda_backward_fused_2d.cu", "msda_backward_fused_3d.cu"),

@@ -584,7 +584,14 @@ cudaError_t forward_nd(const Params &p, cudaStream_t s) {
         if (p.L == 1 && p.P == 4) return launch_tiled_split<DT, G, NDIM, 1, 4>(p, s);
     }
     if constexpr (G >= 2 && G <= 16 && G * 16 >= Shape<NDIM, DT>::VB) {
-        if (p.L * p.P <= kRtMaxSamples) return launch_tiled_rt<DT, G, NDIM>(p, s);
+        // the runtime-(L, P) instantiations live in msda_forward_rt_*.cu (compiled in
+        // parallel with these)
+        if (p.L * p.P <= kRtMaxSamples) {
+            if constexpr (DT == kF32 && NDIM == 2) return launch_forward_rt_f32_2d(G, p, s);
+            if constexpr (DT == kF32 && NDIM == 3) return launch_forward_rt_f32_3d(G, p, s);
+            if constexpr (DT == kBF16 && NDIM == 2) return launch_forward_rt_bf16_2d(G, p, s);
+            if constexpr (DT == kBF16 && NDIM == 3) return launch_forward_rt_bf16_3d(G, p, s);
+        }
     }
     const long long threads = p.n_items * G;
     const long long blocks = (threads + 255) / 256;

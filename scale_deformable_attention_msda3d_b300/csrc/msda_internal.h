@@ -81,6 +81,12 @@ cudaError_t launch_forward_f32_2d(int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_forward_f32_3d(int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_forward_bf16_2d(int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_forward_bf16_3d(int G, const Params &p, cudaStream_t stream);
+// Runtime-(L, P) form of the tiled forward (msda_forward_rt_*.cu): L * P <= 32, G (lanes
+// per row at 16 bytes per lane) in {2, 4, 8, 16}.
+cudaError_t launch_forward_rt_f32_2d(int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_forward_rt_f32_3d(int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_forward_rt_bf16_2d(int G, const Params &p, cudaStream_t stream);
+cudaError_t launch_forward_rt_bf16_3d(int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_backward_2d(int dtype, int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_backward_3d(int dtype, int G, const Params &p, cudaStream_t stream);
 cudaError_t launch_backward_fused_2d(int dtype, int G, const Params &p, cudaStream_t stream);
