@@ -146,3 +146,14 @@ def test_reference_arm_other_ranks_stay_silent():
     """Under torchrun only rank 0 runs the reference arm; another rank prints nothing."""
     assert _run_bench(["--impl", "reference", "--workload", "tiny2d", "--steps", "3",
                        "--warmup", "3"], {"RANK": "1", "WORLD_SIZE": "2"}) == []
+
+
+def test_config_names_the_query_order_mode():
+    """`--order` (each step) and `--order once` (outside the timed region) are different
+    measurements; the config says which."""
+    w = workloads.WORKLOADS["volume3d"]
+    p = bench.build_parser()
+    assert "each step" in bench.run_config(w, p.parse_args(["--order"]), 1)["query_order"]
+    assert "once per input set" in bench.run_config(w, p.parse_args(["--order", "once"]),
+                                                    1)["query_order"]
+    assert bench.run_config(w, p.parse_args([]), 1)["query_order"] == "as given"
