@@ -358,3 +358,31 @@ def test_runtime_level_point_forward(msda, case):
                                    dtype=dtype, seed=zlib.crc32(repr(case).encode()),
                                    backward=False)
     check_forward(msda, nd, inp, dtype, f"runtime (L, P) fwd {case}")
+
+
+def test_runtime_level_point_forward_modes(msda):
+    """The runtime-(L, P) form under pruning, a query order and a non-default stream: the
+    same results as the pruning oracle, bit-identical ordered and unordered outputs."""
+    torch = pytest.importorskip("torch")
+    for nd, dtype, L, P in ((2, "f32", 4, 8), (3, "bf16", 3, 3)):
+        inp = workloads.random_problem(nd, _shapes_for(nd, L), B=2, Nq=150, M=4, D=32, P=P,
+                                       dtype=dtype, seed=90 + nd, backward=False)
+        d = device_inputs(inp, dtype)
+        a = (d["value"], inp["spatial_shapes"], inp["level_start_index"],
+             d["sampling_locations"], d["attention_weights"])
+        fwd = msda.msda2d_forward if nd == 2 else msda.msda3d_forward
+        fwd_p = msda.msda2d_forward_pruned if nd == 2 else msda.msda3d_forward_pruned
+        fwd_o = msda.msda2d_forward_ordered if nd == 2 else msda.msda3d_forward_ordered
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            plain = fwd(*a, stream=st)
+            pruned = fwd_p(*a, 0.05, stream=st)
+            order = msda.msda_query_order(d["sampling_locations"], stream=st)
+            ordered = fwd_o(*a, order, stream=st)
+        torch.cuda.synchronize()
+        args = (nd, inp["value"], inp["spatial_shapes"], inp["level_start_index"],
+                inp["sampling_locations"], inp["attention_weights"])
+        check(host(plain), oracle.forward(*args), dtype, f"runtime (L, P) {nd}d")
+        check(host(pruned), oracle.forward_pruned(*args, 0.05), dtype, f"runtime pruned {nd}d")
+        assert torch.equal(plain, ordered), f"runtime ordered {nd}d differs from unordered"
