@@ -246,7 +246,7 @@ __device__ __forceinline__ uint4 pack16(const float2 *acc) {
 // their weights set to zero, and every FMA runs.
 constexpr int kFwdBlock = 128;
 template <int NDIM, int DT> struct Shape;
-template <> struct Shape<2, kF32> { static constexpr int VB = 16, AHEAD = 2, MINB = 12; static constexpr bool PRED = true; };
+template <> struct Shape<2, kF32> { static constexpr int VB = 16, AHEAD = 1, MINB = 12; static constexpr bool PRED = true; };
 template <> struct Shape<2, kBF16> { static constexpr int VB = 16, AHEAD = 1, MINB = 10; static constexpr bool PRED = false; };
 template <> struct Shape<3, kF32> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; static constexpr bool PRED = false; };
 template <> struct Shape<3, kBF16> { static constexpr int VB = 32, AHEAD = 1, MINB = 6; static constexpr bool PRED = false; };
