@@ -960,6 +960,12 @@ PROBES = (
                                 "247-row tile"),
     ("tma_gather_l2", 5, 320_000, 1, "cp.async.bulk of random 128-B rows into shared memory, "
                                      "41 MB buffer"),
+    # kind 6: 16 rows per warp and batch, so 2 lanes per row in the rows count
+    ("tma_gather4_l2", 6, 320_000, 2, "tensor-copy four-row gathers (tile::gather4) of random "
+                                      "128-B rows into shared memory, 4 batches of 16 rows in "
+                                      "flight per warp, 41 MB buffer"),
+    ("tma_gather4_hbm", 6, 1 << 24, 2, "tensor-copy four-row gathers of random 128-B rows, "
+                                       "2.1 GB buffer (HBM)"),
 )
 
 
@@ -987,11 +993,11 @@ def run_probes(args):
         threads = lib.msda_probe_block(kind)
         blocks = sms * (2048 // threads)
         buf = torch.zeros(max(n_rows, 1) * 32, dtype=torch.float32, device=dev)
-        if kind in (0, 1, 5):
+        if kind in (0, 1, 5, 6):
             buf.uniform_()
         sink = torch.empty(blocks * threads, dtype=torch.float32, device=dev)
         iters = 256 if kind != 5 else 64
-        rows_per_launch = blocks * threads // lanes * iters if kind != 5 else blocks * threads * iters
+        rows_per_launch = blocks * threads // lanes * iters
 
         def launch(seed):
             rc = lib.msda_probe_launch(kind, ctypes.c_void_p(buf.data_ptr()), n_rows, blocks, iters,

@@ -507,9 +507,18 @@ template <> struct RtShape<2, kBF16> { static constexpr int VB = 16, AHEAD = 1, 
 template <> struct RtShape<3, kF32> { static constexpr int VB = 32, AHEAD = 0, MINB = 5; static constexpr bool PRED = false; };
 template <> struct RtShape<3, kBF16> { static constexpr int VB = 32, AHEAD = 0, MINB = 5; static constexpr bool PRED = false; };
 
+// The launch shape of the compiled (LL > 0) or runtime-(L, P) (LL = 0) form.  The lanes per
+// row (G) of a launch are derived from the same shape's VB, so that the G lanes of a group
+// cover exactly one head's D channels.
+template <int NDIM, int DT, int LL>
+using TiledShape = typename std::conditional<LL == 0, RtShape<NDIM, DT>, Shape<NDIM, DT>>::type;
+
 template <int DT, int G, int NDIM, int LL, int PP, int SPLIT>
 cudaError_t launch_tiled(const Params &p, cudaStream_t s) {
-    using SH = typename std::conditional<LL == 0, RtShape<NDIM, DT>, Shape<NDIM, DT>>::type;
+    using SH = TiledShape<NDIM, DT, LL>;
+    // a lane group must span one head's channels exactly: a wider group would read the
+    // next head's (or past the row's) bytes
+    if (static_cast<long long>(G) * SH::VB * p.M != p.row_bytes) return cudaErrorInvalidValue;
     const long long threads = p.n_items * G * SPLIT;
     const long long blocks = (threads + kFwdBlock - 1) / kFwdBlock;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -535,7 +544,7 @@ cudaError_t launch_tiled(const Params &p, cudaStream_t s) {
 // G16 = lanes per row at 16 bytes per lane; the kernel uses G = row bytes / VB lanes.
 template <int DT, int G16, int NDIM, int LL, int PP>
 cudaError_t launch_tiled_split(const Params &p, cudaStream_t s) {
-    constexpr int VB = Shape<NDIM, DT>::VB;
+    constexpr int VB = TiledShape<NDIM, DT, LL>::VB;
     constexpr int G = G16 * 16 / VB;
     static_assert(G >= 1, "rows narrower than one lane's slice take the generic path");
     const int split = pick_split<G, LL * PP, NDIM>(p.n_items);
@@ -565,7 +574,7 @@ int pick_split_rt(int S, long long n_items) {
 
 template <int DT, int G16, int NDIM>
 cudaError_t launch_tiled_rt(const Params &p, cudaStream_t s) {
-    constexpr int VB = Shape<NDIM, DT>::VB;
+    constexpr int VB = TiledShape<NDIM, DT, 0>::VB;
     constexpr int G = G16 * 16 / VB;
     const int split = pick_split_rt<G, NDIM>(p.L * p.P, p.n_items);
     if constexpr (G <= 16) {
@@ -583,7 +592,7 @@ cudaError_t forward_nd(const Params &p, cudaStream_t s) {
         if (p.L == 4 && p.P == 4) return launch_tiled_split<DT, G, NDIM, 4, 4>(p, s);
         if (p.L == 1 && p.P == 4) return launch_tiled_split<DT, G, NDIM, 1, 4>(p, s);
     }
-    if constexpr (G >= 2 && G <= 16 && G * 16 >= Shape<NDIM, DT>::VB) {
+    if constexpr (G >= 2 && G <= 16 && G * 16 >= TiledShape<NDIM, DT, 0>::VB) {
         // the runtime-(L, P) instantiations live in msda_forward_rt_*.cu (compiled in
         // parallel with these)
         if (p.L * p.P <= kRtMaxSamples) {

@@ -14,11 +14,16 @@
 //                       shared-memory load, add, store)
 //   tma_gather_rows     random rows copied into shared memory by cp.async.bulk (one
 //                       128-byte bulk copy per row, completion on an mbarrier)
+//   tma_gather4_rows    random rows copied into shared memory by the tensor copy's
+//                       four-row gather mode (cp.async.bulk.tensor ... tile::gather4: four
+//                       rows of a 2D tensor map per copy), four stages per warp in flight,
+//                       each row then read from shared memory by the warp
 //
 // Every wait is bounded: a wait that runs out of iterations sets *err and the kernel
 // returns after waiting (again bounded) for its own copies.  The host side only launches
 // kernels; timing is done by the caller with CUDA events.
 #include <cstdint>
+#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
 #include <cuda_runtime.h>
 
 namespace {
@@ -181,13 +186,117 @@ __global__ void __launch_bounds__(128) tma_gather_rows(const char *__restrict__ 
     sink[blockIdx.x * blockDim.x + threadIdx.x] = acc;
 }
 
+// Four-row gathers: each warp keeps kG4Stages batches in flight; a batch is kG4Ops
+// tile::gather4 copies (issued by lanes 0 .. kG4Ops-1, 4 rows of 128 bytes each) completing
+// on the stage's mbarrier.  The warp then reads the batch's rows from shared memory (one
+// 16-byte slice per lane per row group, as the forward's lane groups would) and re-issues
+// the stage.
+constexpr int kG4Warps = 4, kG4Stages = 4, kG4Ops = 4;
+constexpr unsigned kG4BatchBytes = kG4Ops * 4 * 128;
+
+__global__ void __launch_bounds__(kG4Warps * 32)
+tma_gather4_rows(const __grid_constant__ CUtensorMap map, unsigned n_rows, int iters,
+                 unsigned seed, float *sink, int *err) {
+    __shared__ __align__(128) char rows[kG4Warps][kG4Stages][kG4BatchBytes];
+    __shared__ __align__(8) unsigned long long bars[kG4Warps][kG4Stages];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t bar0 = static_cast<uint32_t>(__cvta_generic_to_shared(&bars[warp][0]));
+    if (lane == 0) {
+        for (int s = 0; s < kG4Stages; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar0 + 8u * s) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    const unsigned gw = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    // batch i goes to stage i % kG4Stages
+    auto issue = [&](int i) {
+        const int s = i % kG4Stages;
+        const uint32_t bar = bar0 + 8u * s;
+        if (lane == 0)
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                         :: "r"(bar), "r"(kG4BatchBytes) : "memory");
+        __syncwarp();
+        if (lane < kG4Ops) {
+            const unsigned key = (gw * 7919u + i * 104729u + lane * 31u + seed) * 4u;
+            const int r0 = static_cast<int>(pick(key, n_rows));
+            const int r1 = static_cast<int>(pick(key + 1u, n_rows));
+            const int r2 = static_cast<int>(pick(key + 2u, n_rows));
+            const int r3 = static_cast<int>(pick(key + 3u, n_rows));
+            const uint32_t dst =
+                static_cast<uint32_t>(__cvta_generic_to_shared(&rows[warp][s][lane * 4 * 128]));
+            asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4"
+                         ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+                         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(&map)), "r"(0), "r"(r0),
+                            "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+                         : "memory");
+        }
+    };
+    int issued = 0;
+    for (; issued < kG4Stages && issued < iters; ++issued) issue(issued);
+    float acc = 0.f;
+    bool ok = true;
+    int i = 0;
+    for (; i < iters; ++i) {
+        const int s = i % kG4Stages;
+        ok = mbar_wait(bar0 + 8u * s, (i / kG4Stages) & 1);
+        if (!ok) break;
+        const float4 *st = reinterpret_cast<const float4 *>(&rows[warp][s][0]);
+#pragma unroll
+        for (int k = 0; k < static_cast<int>(kG4BatchBytes / 512); ++k) {
+            const float4 v = st[k * 32 + lane];
+            acc += (v.x + v.y) + (v.z + v.w);
+        }
+        __syncwarp();
+        // the stage's next copies (async proxy) overwrite what was just read
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (issued < iters) issue(issued++);
+    }
+    if (!ok) {
+        atomicExch(err, 1);
+        // batches i .. issued-1 may still be in flight: wait for them (bounded) before the
+        // block's shared memory goes away
+        for (int j = i; j < issued; ++j)
+            (void)mbar_wait(bar0 + 8u * (j % kG4Stages), (j / kG4Stages) & 1);
+    }
+    sink[blockIdx.x * blockDim.x + threadIdx.x] = acc;
+}
+
+// The tensor map of a buffer of n_rows rows of 32 fp32 (128 bytes), one row per box, for
+// the four-row gather.  The encoder comes from the driver at run time (no libcuda link).
+cudaError_t row_tensor_map(void *buf, unsigned n_rows, CUtensorMap *map) {
+    using Encode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static Encode encode = nullptr;
+    if (encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn,
+                                                               12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return e != cudaSuccess ? e : cudaErrorNotSupported;
+        encode = reinterpret_cast<Encode>(fn);
+    }
+    const cuuint64_t dims[2] = {32, n_rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {32, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, buf, dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 extern "C" {
 
-// kind: 0 gather16, 1 gather32, 2 reduce, 3 smem atomic, 4 smem owner, 5 tma gather.
-// Returns the CUDA launch status.  buf / n_rows: the row buffer (unused by kinds 3, 4);
-// sink: one float per thread of the grid (blocks * threads); err: one int (kind 5).
+// kind: 0 gather16, 1 gather32, 2 reduce, 3 smem atomic, 4 smem owner, 5 tma gather,
+// 6 tma four-row gather.  Returns the CUDA launch status.  buf / n_rows: the row buffer
+// (unused by kinds 3, 4); sink: one float per thread of the grid (blocks * threads); err:
+// one int (kinds 5, 6).
 int msda_probe_launch(int kind, void *buf, unsigned n_rows, int blocks, int iters,
                       unsigned seed, float *sink, int *err, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -198,12 +307,23 @@ int msda_probe_launch(int kind, void *buf, unsigned n_rows, int blocks, int iter
         case 3: smem_atomic_rows<<<blocks, 256, 0, s>>>(iters, seed, sink); break;
         case 4: smem_owner_rows<<<blocks, 256, 0, s>>>(iters, seed, sink); break;
         case 5: tma_gather_rows<<<blocks, 128, 0, s>>>(static_cast<const char *>(buf), n_rows, iters, seed, sink, err); break;
+        case 6: {
+            // rows must start 16-byte aligned for the tensor map (the buffer is 256-byte
+            // aligned, rows are 128 bytes)
+            if ((reinterpret_cast<uintptr_t>(buf) & 127u) != 0 || n_rows == 0)
+                return static_cast<int>(cudaErrorInvalidValue);
+            CUtensorMap map;
+            const cudaError_t e = row_tensor_map(buf, n_rows, &map);
+            if (e != cudaSuccess) return static_cast<int>(e);
+            tma_gather4_rows<<<blocks, kG4Warps * 32, 0, s>>>(map, n_rows, iters, seed, sink, err);
+            break;
+        }
         default: return static_cast<int>(cudaErrorInvalidValue);
     }
     return static_cast<int>(cudaGetLastError());
 }
 
 // Threads per block of a probe kind (the caller sizes sink as blocks * this).
-int msda_probe_block(int kind) { return kind == 5 ? 128 : 256; }
+int msda_probe_block(int kind) { return kind == 5 ? 128 : kind == 6 ? kG4Warps * 32 : 256; }
 
 }  // extern "C"
