@@ -16,14 +16,16 @@
 //   j of the group owns samples j, G + j, 2G + j, ...: it reads their locations and
 //   weights, computes their taps and leaves each sample's tap record (row, a, fractions,
 //   validity bits) in shared memory for the group.  Every lane loads the in-level corner
-//   rows of each sample (predicated, no zeroed registers) and forms its partial dot
-//   products <g, v_c> over its channels; after each batch of G samples a butterfly
-//   reduce-scatter leaves each sample's full dot products on its owner, which writes grad_A
-//   and grad_loc.  grad_value goes through 16-byte red.global.add.v4.f32.
+//   rows of each sample (predicated, no zeroed registers), forms its partial dot products
+//   <g, v_c> over its channels and folds them into partial grad_A and grad_x, grad_y
+//   (, grad_z), which are linear in them; after each batch of G samples a butterfly
+//   reduce-scatter leaves each sample's gradient sums on its owner, which writes grad_A
+//   and grad_loc.  grad_value goes through 16-byte red.global.add.v4.f32, issued so that
+//   the lanes of one instruction cover a contiguous run of the row (add_global_runs).
 //   (Accumulating small levels in shared memory first was measured and dropped: on this
 //   part shared-memory fp32 atomics ran about ten times slower than the L2 reductions.)
 // * bwd{2,3}d_generic (any L, P): every lane of the group computes every sample, reduces
-//   grad_A / grad_loc with xor shuffles and scatters with red.global.add.v4.f32.
+//   grad_A / grad_loc with xor shuffles and scatters with red.global.add.v4.f32 in runs.
 // With FUSED (the backward of the fused-prologue forward) the kernels form the locations
 // and softmax weights from reference points, offsets and logits as the fused forward does,
 // and write offset gradients (d location / d offset = 1 / extent); bwd_tiled also forms
@@ -36,12 +38,42 @@ namespace msda {
 
 namespace {
 
-// grad_value += wgt * g over the N channels a lane owns (N/4 vector reductions).
-template <int N>
-__device__ __forceinline__ void scatter(float *dst, float wgt, const float (&g)[N]) {
+// grad_value += wgt * gr over this lane's N channels of one corner row, laid out in runs:
+// reduction k (k < N / 4) of lane `sub` covers channels k * 4G + 4 sub .. + 3, so the G
+// lanes of one instruction fill a contiguous 16 G-byte run of the fp32 row.  dst points at
+// channel 4 sub of the row; gr holds those channels of grad_out (see run_channels).
+template <int N, int G>
+__device__ __forceinline__ void add_global_runs(float *dst, float wgt, const float (&gr)[N]) {
 #pragma unroll
-    for (int i = 0; i < N; i += 4)
-        red_add_v4(dst + i, wgt * g[i], wgt * g[i + 1], wgt * g[i + 2], wgt * g[i + 3]);
+    for (int k = 0; k < N / 4; ++k)
+        red_add_v4(dst + k * 4 * G, wgt * gr[4 * k], wgt * gr[4 * k + 1], wgt * gr[4 * k + 2],
+                   wgt * gr[4 * k + 3]);
+}
+
+// The grad_out channels of lane `sub`'s reductions (channels k * 4G + 4 sub .. + 3), from
+// the item's grad_out row: for fp32 (N = 4) they are the lane's own 16 bytes; for bf16
+// (N = 8) two 8-byte pieces.  Why runs: a lane's 8 bf16 channels are 32 bytes of fp32
+// gradient, and two reductions over the lanes' interleaved halves would write 16 bytes
+// into each 32-byte sector of the line twice; the L2 reduction units work per sector, so
+// runs of whole sectors halve their work.
+template <int DT, int G>
+__device__ __forceinline__ void run_channels(const char *go_row, int sub,
+                                             const float (&g)[Vec<DT>::N],
+                                             float (&gr)[Vec<DT>::N]) {
+    constexpr int N = Vec<DT>::N;
+    if constexpr (N == 4) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) gr[i] = g[i];
+    } else {
+#pragma unroll
+        for (int k = 0; k < N / 4; ++k) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(go_row) + k * G + sub);
+            gr[4 * k] = __uint_as_float(u.x << 16);
+            gr[4 * k + 1] = __uint_as_float(u.x & 0xffff0000u);
+            gr[4 * k + 2] = __uint_as_float(u.y << 16);
+            gr[4 * k + 3] = __uint_as_float(u.y & 0xffff0000u);
+        }
+    }
 }
 
 template <int N>
@@ -73,9 +105,12 @@ bwd2d_generic(const __grid_constant__ Params p) {
     const long long rowf = static_cast<long long>(p.M) * p.D;  // grad_value row stride (floats)
     const char *vb = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
                      static_cast<long long>(m) * (rb / p.M) + sub * 16;
-    float *gvb = p.grad_value + (b * p.Nin) * rowf + static_cast<long long>(m) * p.D + sub * N;
-    float g[N];
-    unpack(ldg16(static_cast<const char *>(p.grad_out) + item * (rb / p.M) + sub * 16), g);
+    // channel 4 sub of the head's grad_value row (reductions in runs, see add_global_runs)
+    float *gvb = p.grad_value + (b * p.Nin) * rowf + static_cast<long long>(m) * p.D + sub * 4;
+    const char *go_row = static_cast<const char *>(p.grad_out) + item * (rb / p.M);
+    float g[N], gr[N];
+    unpack(ldg16(go_row + sub * 16), g);
+    run_channels<DT, G>(go_row, sub, g, gr);
     const long long s0 = item * L * P;
     const float2 *lp = reinterpret_cast<const float2 *>(p.loc) + s0;
     float zmax = 0.f, zsum = 1.f;
@@ -137,10 +172,10 @@ bwd2d_generic(const __grid_constant__ Params p) {
                     p.grad_loc[2 * s + 1] = any ? a * gy * eH : 0.f;
                 }
                 float *d = gl + r00 * rowf;
-                if (ok00) scatter<N>(d, a * (wy0 * wx0), g);
-                if (ok01) scatter<N>(d + rowf, a * (wy0 * fx), g);
-                if (ok10) scatter<N>(d + W * rowf, a * (fy * wx0), g);
-                if (ok11) scatter<N>(d + (W + 1) * rowf, a * (fy * fx), g);
+                if (ok00) add_global_runs<N, G>(d, a * (wy0 * wx0), gr);
+                if (ok01) add_global_runs<N, G>(d + rowf, a * (wy0 * fx), gr);
+                if (ok10) add_global_runs<N, G>(d + W * rowf, a * (fy * wx0), gr);
+                if (ok11) add_global_runs<N, G>(d + (W + 1) * rowf, a * (fy * fx), gr);
             }
         }
     }
@@ -164,9 +199,12 @@ bwd3d_generic(const __grid_constant__ Params p) {
     const long long rowf = static_cast<long long>(p.M) * p.D;
     const char *vb = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
                      static_cast<long long>(m) * (rb / p.M) + sub * 16;
-    float *gvb = p.grad_value + (b * p.Nin) * rowf + static_cast<long long>(m) * p.D + sub * N;
-    float g[N];
-    unpack(ldg16(static_cast<const char *>(p.grad_out) + item * (rb / p.M) + sub * 16), g);
+    // channel 4 sub of the head's grad_value row (reductions in runs, see add_global_runs)
+    float *gvb = p.grad_value + (b * p.Nin) * rowf + static_cast<long long>(m) * p.D + sub * 4;
+    const char *go_row = static_cast<const char *>(p.grad_out) + item * (rb / p.M);
+    float g[N], gr[N];
+    unpack(ldg16(go_row + sub * 16), g);
+    run_channels<DT, G>(go_row, sub, g, gr);
     const long long s0 = item * L * P;
     float zmax = 0.f, zsum = 1.f;
     if constexpr (FUSED) logit_stats(p.attn + s0, L * P, zmax, zsum);
@@ -244,7 +282,8 @@ bwd3d_generic(const __grid_constant__ Params p) {
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
-                    if (ok[c]) scatter<N>(dst + off[c] * rowf, a * (wz[dz] * wy[dy] * wx[dx]), g);
+                    if (ok[c])
+                        add_global_runs<N, G>(dst + off[c] * rowf, a * (wz[dz] * wy[dy] * wx[dx]), gr);
                 }
             }
         }
@@ -271,13 +310,6 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[G][K], int sub) {
     }
 }
 
-// grad_value += wgt * g over this lane's N channels of one corner row.
-template <int N>
-__device__ __forceinline__ void add_global(float *dst, float wgt, const float (&g)[N]) {
-#pragma unroll
-    for (int i = 0; i < N; i += 4)
-        red_add_v4(dst + i, wgt * g[i], wgt * g[i + 1], wgt * g[i + 2], wgt * g[i + 3]);
-}
 template <int DT, int G, int NDIM, int LL, int PP, int BT, bool FUSED>
 __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
     constexpr int N = Vec<DT>::N;  // channels per lane (16 bytes of value)
@@ -301,8 +333,9 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
     const char *vbase = static_cast<const char *>(p.value) + (b * p.Nin) * rb +
                         static_cast<long long>(m) * (rb / p.M) + sub * 16;
     constexpr int GS = 4 / Vec<DT>::ESIZE;  // grad_value (fp32) bytes per value byte
+    // channel 4 sub of the head's grad_value row (reductions in runs, see add_global_runs)
     char *gbase = reinterpret_cast<char *>(p.grad_value + (b * p.Nin) * rowf +
-                                           static_cast<long long>(m) * D + sub * N);
+                                           static_cast<long long>(m) * D + sub * 4);
     // tap records of the CTA's queries (see common.cuh): row, a, fx, fy (+ fz), validity
     constexpr int ISTR = tap_slot(S - 1) + 2;
     constexpr int OKB = NDIM == 2 ? 4 : 8;  // validity bits under a packed row
@@ -316,8 +349,10 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
         const bool active = q < q_hi;
         if (!active) q = q_hi - 1;  // recompute a real query, write nothing
         const long long item = (b * p.Nq + q) * p.M + m;
-        float g[N];
-        unpack(ldg16(static_cast<const char *>(p.grad_out) + item * (rb / p.M) + sub * 16), g);
+        const char *go_row = static_cast<const char *>(p.grad_out) + item * (rb / p.M);
+        float g[N], gr[N];
+        unpack(ldg16(go_row + sub * 16), g);
+        run_channels<DT, G>(go_row, sub, g, gr);
         // fused: softmax weights of the samples this lane owns (max and sum over the group)
         // and their grad_A, kept until the item's logit gradients can be formed
         float av[NB], gAs[NB];
@@ -343,9 +378,9 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
             for (int bt = 0; bt < NB; ++bt) av[bt] = __fdiv_rn(av[bt], sum);
         }
 
-        // 1. taps of the samples this lane owns (bt * G + sub), kept for the owner's
-        //    gradient formulas and left in shared memory for the group
-        float frac[NB][NDIM], aw[NB];
+        // 1. taps of the samples this lane owns (bt * G + sub), left in shared memory for
+        //    the group; the owner keeps its weight and validity bits for its own outputs
+        float aw[NB];
         unsigned okw[NB];
 #pragma unroll
         for (int bt = 0; bt < NB; ++bt) {
@@ -371,7 +406,8 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
                 a = __ldcs(p.attn + item * S + so);
             }
             Taps<NC> mine;
-            make_taps(p, so / PP, xyz, a, mine, frac[bt]);
+            float fr[NDIM];
+            make_taps(p, so / PP, xyz, a, mine, fr);
             aw[bt] = a;
             okw[bt] = mine.ok;
             if (own < S) {
@@ -380,27 +416,30 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
                 const int rbits =
                     p.pack_taps ? static_cast<int>((static_cast<unsigned>(mine.row) << OKB) | mine.ok)
                                 : mine.row;
-                rec[j] = make_float4(__int_as_float(rbits), a, frac[bt][0], frac[bt][1]);
+                rec[j] = make_float4(__int_as_float(rbits), a, fr[0], fr[1]);
                 if (!p.pack_taps) rec_ok[j] = mine.ok;
-                if constexpr (NDIM == 3) rec_z[j] = frac[bt][2];
+                if constexpr (NDIM == 3) rec_z[j] = fr[2];
             }
         }
         __syncwarp();
 
-        // 2. per batch of G samples: corner rows (in-level corners only), partial dot
-        //    products <g, v_c> over this lane's channels, grad_value reductions; then the
-        //    owner of each sample gets its full dot products and writes grad_A, grad_loc
+        // 2. per batch of G samples: corner rows (in-level corners only), the dot products
+        //    d_c = <g, v_c> over this lane's channels, grad_value reductions.  A sample's
+        //    gradients are linear in its dot products -- grad_A = sum_c w_c d_c and
+        //    grad_x = sum_c (dw_c / dx) d_c, likewise y (and z), with w_c the bilinear
+        //    (trilinear) weights without A -- so each lane folds its partial dot products
+        //    into partial gradients at once, and one reduce-scatter over the group hands the
+        //    owner of each sample its totals.
+        constexpr int NG = 1 + NDIM;  // grad_A, grad_x, grad_y (, grad_z)
 #pragma unroll
         for (int bt = 0; bt < NB; ++bt) {
-            float dp[G][NC];  // partial <g, v_c> of every sample of the batch
+            float pg[G][NG];  // this lane's partial gradients of every sample of the batch
 #pragma unroll
             for (int j = 0; j < G; ++j) {
                 const int s = bt * G + j;
-                if (s >= S) {
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) dp[j][c] = 0.f;
-                    continue;
-                }
+                for (int k = 0; k < NG; ++k) pg[j][k] = 0.f;
+                if (s >= S) continue;
                 const int jr = grp * ISTR + tap_slot(s);
                 const float4 rr = rec[jr];
                 const int rv = __float_as_int(rr.x);
@@ -408,8 +447,17 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
                 const unsigned ok = p.pack_taps ? static_cast<unsigned>(rv) & ((1u << OKB) - 1u)
                                                 : rec_ok[jr];
                 float w[NC];
-                if constexpr (NDIM == 2) tap_weights(rr.y, rr.z, rr.w, w);
-                else tap_weights(rr.y, rr.z, rr.w, rec_z[jr], w);
+                float fz = 0.f;
+                if constexpr (NDIM == 2) {
+                    tap_weights(rr.y, rr.z, rr.w, w);
+                } else {
+                    fz = rec_z[jr];
+                    tap_weights(rr.y, rr.z, rr.w, fz, w);
+                }
+                // the per-axis factors of the corner weights, without A
+                const float wx[2] = {1.f - rr.z, rr.z};
+                const float wy[2] = {1.f - rr.w, rr.w};
+                const float wz[2] = {NDIM == 3 ? 1.f - fz : 1.f, NDIM == 3 ? fz : 1.f};
                 const int l = s / PP;
                 // value and grad_value addresses of corner 0 and of the corner one image row
                 // further; grad_value rows are fp32, GS times as wide as value rows
@@ -435,35 +483,23 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
 #pragma unroll
                         for (int i = 0; i < N; ++i) d = fmaf(g[i], v[i], d);
                     }
-                    dp[j][c] = d;
+                    const float sx = dx ? 1.f : -1.f, sy = dy ? 1.f : -1.f, sz = dz ? 1.f : -1.f;
+                    pg[j][0] = fmaf(wz[dz] * wy[dy] * wx[dx], d, pg[j][0]);
+                    pg[j][1] = fmaf(sx * wz[dz] * wy[dy], d, pg[j][1]);
+                    pg[j][2] = fmaf(sy * wz[dz] * wx[dx], d, pg[j][2]);
+                    if constexpr (NDIM == 3) pg[j][3] = fmaf(sz * wy[dy] * wx[dx], d, pg[j][3]);
                     if (active && in) {
                         char *dst = gy[dy] + (dz ? p.sz[l] * GS : 0) + (dx ? rb * GS : 0);
-                        add_global<N>(reinterpret_cast<float *>(dst), w[c], g);
+                        add_global_runs<N, G>(reinterpret_cast<float *>(dst), w[c], gr);
                     }
                 }
             }
-            reduce_scatter<G, NC>(dp, sub);
+            reduce_scatter<G, NG>(pg, sub);
             const int own = bt * G + sub;
             if (active && own < S) {
-                // dp[0][c] = <g, v_c> of sample `own`; corner weight derivatives from frac
+                // pg[0] = the gradients of sample `own` before the factors A and extent
                 const long long s = item * S + own;
-                const float *fr = frac[bt];
-                float wx[2], wy[2], wz[2];
-                wx[0] = 1.f - fr[0]; wx[1] = fr[0];
-                wy[0] = 1.f - fr[1]; wy[1] = fr[1];
-                wz[0] = 1.f; wz[1] = 1.f;
-                if constexpr (NDIM == 3) { wz[0] = 1.f - fr[2]; wz[1] = fr[2]; }
-                float gA = 0.f, gx = 0.f, gy = 0.f, gz = 0.f;
-#pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    const int dx = c & 1, dy = (c >> 1) & 1, dz = c >> 2;
-                    const float d = dp[0][c];
-                    const float sx = dx ? 1.f : -1.f, sy = dy ? 1.f : -1.f, sz = dz ? 1.f : -1.f;
-                    gA = fmaf(wz[dz] * wy[dy] * wx[dx], d, gA);
-                    gx = fmaf(sx * wz[dz] * wy[dy], d, gx);
-                    gy = fmaf(sy * wz[dz] * wx[dx], d, gy);
-                    if constexpr (NDIM == 3) gz = fmaf(sz * wy[dy] * wx[dx], d, gz);
-                }
+                const float gA = pg[0][0], gx = pg[0][1], gy = pg[0][2];
                 const bool any = okw[bt] != 0u;
                 const int l = own / PP;
                 const float a = aw[bt];
@@ -473,7 +509,7 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
                 p.grad_loc[NDIM * s] = any ? a * gx * (FUSED ? 1.f : p.fW[l]) : 0.f;
                 p.grad_loc[NDIM * s + 1] = any ? a * gy * (FUSED ? 1.f : p.fH[l]) : 0.f;
                 if constexpr (NDIM == 3)
-                    p.grad_loc[NDIM * s + 2] = any ? a * gz * (FUSED ? 1.f : p.fZ[l]) : 0.f;
+                    p.grad_loc[NDIM * s + 2] = any ? a * pg[0][NDIM] * (FUSED ? 1.f : p.fZ[l]) : 0.f;
             }
         }
         if constexpr (FUSED) {
