@@ -46,6 +46,10 @@ UNIT = "samples/s"
 NOMINAL_HBM_GBS = 7700.0  # B300 HBM3e nominal bandwidth
 FALLBACK_HBM_GBS = 6400.0
 L1_WAVEFRONT_BYTES = 128   # bytes one L1 data-pipe wavefront delivers; one per SM clock
+# Rate of the L2 reduction units in 32-byte sector updates per second: the reduce_l2 probe
+# (`bench.py --probe reduce_l2`: red.global.add.v4.f32 of random 128-byte rows, 8 lanes
+# per row, four whole sectors per request) measured 49.6 G rows/s on a B300.
+L2_RED_SECTORS_PER_S = 4 * 49.6e9
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SRC_DIR = os.path.join(ROOT, "scale_deformable_attention_msda3d_b300", "csrc")
 
@@ -141,6 +145,21 @@ def l1_ceiling(w, corner_rows: int, wavefronts, sm_count: int, sm_mhz, launch_s:
             "hbm_frac_ceiling": alg_bytes / (rows_floor * 1e-6) / 1e9 / hbm_peak_gbs,
             "source": "rows counted on the host from the inputs; wavefronts from the ncu "
                       "summary of the current kernel sources (null when none matches)"}
+
+
+def l2_reduction_ceiling(w, corner_rows: int, launch_s: float) -> dict:
+    """The L2-side ceiling of the backward: every in-level corner row of every sample adds
+    its weighted grad_out into one D-channel fp32 row of grad_value with vector reductions
+    issued in runs of whole 32-byte sectors, D * 4 / 32 sector updates per row.  floor_us is
+    the time those updates need at the rate the reduce_l2 probe measured
+    (L2_RED_SECTORS_PER_S); frac = that floor over the measured launch time."""
+    sectors = corner_rows * max(1, -(-(w.D * 4) // 32))
+    floor_us = sectors / L2_RED_SECTORS_PER_S * 1e6
+    return {"bound": "l2_reductions", "unit": "32-byte sector updates",
+            "sector_updates_per_launch": sectors, "rate_per_s": L2_RED_SECTORS_PER_S,
+            "floor_us": floor_us, "frac": floor_us / (launch_s * 1e6),
+            "source": "rows counted on the host from the inputs; the rate measured by the "
+                      "reduce_l2 probe on a B300 (49.6 G 128-byte rows/s)"}
 
 
 def l2_bytes(dev) -> int:
@@ -712,6 +731,8 @@ def run_ours(args):
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.4 TB/s",
                      "secondary": secondary,
+                     **({"reductions": l2_reduction_ceiling(w, counts[1], per_launch_s)}
+                        if w.backward else {}),
                      "nominal": {"peak": NOMINAL_HBM_GBS, "frac": achieved / NOMINAL_HBM_GBS,
                                  "note": "HBM3e nominal, the metric's ~8 TB/s"},
                      "algorithmic_bytes_per_launch": ab["total"],

@@ -142,6 +142,20 @@ def test_corner_row_count_and_l1_ceiling():
     assert abs(c["floor_us"] - 15.0) < 1e-9 and abs(c["frac"] - 0.75) < 1e-12
 
 
+def test_l2_reduction_ceiling():
+    """The backward's L2 ceiling: D * 4 / 32 sector updates per in-level corner row (fp32
+    grad_value rows, reductions in runs of whole sectors) at the probe's measured rate."""
+    w = workloads.WORKLOADS["volume3d_bwd"]                 # D = 32: four sectors per row
+    rows = 1_000_000
+    c = bench.l2_reduction_ceiling(w, rows, 40e-6)
+    assert c["sector_updates_per_launch"] == 4 * rows
+    want_us = 4 * rows / bench.L2_RED_SECTORS_PER_S * 1e6
+    assert abs(c["floor_us"] - want_us) < 1e-9
+    assert abs(c["frac"] - want_us / 40.0) < 1e-12
+    w8 = workloads.Workload("t", 2, 1, ((4, 4),), 3, 1, 8, 1, "bf16", 1, backward=True)
+    assert bench.l2_reduction_ceiling(w8, 10, 1e-6)["sector_updates_per_launch"] == 10
+
+
 def test_reference_arm_other_ranks_stay_silent():
     """Under torchrun only rank 0 runs the reference arm; another rank prints nothing."""
     assert _run_bench(["--impl", "reference", "--workload", "tiny2d", "--steps", "3",
