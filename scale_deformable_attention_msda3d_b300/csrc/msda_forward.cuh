@@ -485,12 +485,16 @@ fwd_tiled(const __grid_constant__ Params p) {
 
 // Lane groups per item for the compiled path.  Narrow rows (few lanes per row) split an
 // item's samples until one lane computes the taps of at most MAX_SPL samples (their
-// registers would spill otherwise); then the split grows while the launch would leave the
-// GPU short of resident warps.
+// registers would spill otherwise); then the split grows while the launch has fewer than
+// kWantThreads threads.
+// kWantThreads: 1024 threads per SM of the B300, half its resident threads.  Measured on
+// the decoder-shaped forward (19,200 items, 4 lanes per row): split 2 (153,600 threads)
+// ran at 11.9 us, split 4 (two full waves, the earlier rule) at 12.7 us, split 1 at 14.4.
+constexpr long long kWantThreads = 148LL * 1024;
+
 template <int G, int S, int NDIM>
 int pick_split(long long n_items) {
     constexpr int MAX_SPL = NDIM == 2 ? 4 : 2;
-    constexpr long long kWantThreads = 148LL * 2048 * 2;  // two full waves of the B300's SMs
     auto can_double = [](int split) { return split < 4 && G * split * 2 <= 32 && S % (split * 2) == 0; };
     int split = 1;
     while (can_double(split) && S / split > MAX_SPL * G) split *= 2;
@@ -564,7 +568,6 @@ constexpr int kRtMaxSamples = 32;
 template <int G, int NDIM>
 int pick_split_rt(int S, long long n_items) {
     constexpr int MAX_SPL = NDIM == 2 ? 4 : 2;
-    constexpr long long kWantThreads = 148LL * 2048 * 2;
     auto can_double = [S](int split) { return split < 4 && G * split * 2 <= 32 && S % (split * 2) == 0; };
     int split = 1;
     while (can_double(split) && S / split > MAX_SPL * G) split *= 2;
