@@ -16,11 +16,11 @@
 //   j of the group owns samples j, G + j, 2G + j, ...: it reads their locations and
 //   weights, computes their taps and leaves each sample's tap record (row, a, fractions,
 //   validity bits) in shared memory for the group.  Every lane loads the in-level corner
-//   rows of each sample (predicated, no zeroed registers), forms its partial dot products
-//   <g, v_c> over its channels and folds them into partial grad_A and grad_x, grad_y
-//   (, grad_z), which are linear in them; after each batch of G samples a butterfly
-//   reduce-scatter leaves each sample's gradient sums on its owner, which writes grad_A
-//   and grad_loc.  grad_value goes through 16-byte red.global.add.v4.f32, issued so that
+//   rows of each sample (predicated, no zeroed registers) and forms its partial dot
+//   products <g, v_c> over its channels (in 3D folded at once into partial grad_A, grad_x,
+//   grad_y, grad_z, which are linear in them); after each batch of G samples a butterfly
+//   reduce-scatter leaves each sample's sums on its owner, which writes grad_A and
+//   grad_loc.  grad_value goes through 16-byte red.global.add.v4.f32, issued so that
 //   the lanes of one instruction cover a contiguous run of the row (add_global_runs).
 //   (Accumulating small levels in shared memory first was measured and dropped: on this
 //   part shared-memory fp32 atomics ran about ten times slower than the L2 reductions.)
