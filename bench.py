@@ -807,7 +807,7 @@ def run_e2e(msda, w, inp, dev, args, world):
     comp_done = [torch.cuda.Event() for _ in range(nbuf)]
     out_done = [torch.cuda.Event() for _ in range(nbuf)]
 
-    def one(i):
+    def one(i, compute=True):
         k = i % nbuf
         d, od, oh = dins[k], outs_d[k], outs_h[k]
         if i >= nbuf:
@@ -819,7 +819,9 @@ def run_e2e(msda, w, inp, dev, args, world):
         s_comp.wait_event(in_done[k])
         if i >= nbuf:
             s_comp.wait_event(out_done[k])      # step i - nbuf's result has been downloaded
-        if not w.backward:
+        if not compute:
+            pass
+        elif not w.backward:
             fn(d["value"], shapes, starts, d["loc"], d["attn"], out=od[0], stream=s_comp)
         else:
             fn(d["value"], shapes, starts, d["loc"], d["attn"], d["grad_out"],
@@ -848,9 +850,24 @@ def run_e2e(msda, w, inp, dev, args, world):
     wall = time.perf_counter() - t0
     t = max(ev0.elapsed_time(ev1) / 1e3, 0.0)
     value, t_max = aggregate(max(t, wall), w.samples, steps, world)
+    # The same pipeline with the copies alone (no libmsda call), after the timed region:
+    # the floor the host link sets for these bytes (uploads and downloads share it).
+    for i in range(3):
+        one(i, compute=False)
+    torch.cuda.synchronize(dev)
+    ev2 = torch.cuda.Event(enable_timing=True)
+    ev3 = torch.cuda.Event(enable_timing=True)
+    ev2.record(s_in)
+    for i in range(steps):
+        one(i, compute=False)
+    ev3.record(s_out)
+    torch.cuda.synchronize(dev)
+    copies_ms = ev2.elapsed_time(ev3) / steps
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": t_max * 1e3 / steps,
+            "copies_only_ms_per_step": copies_ms,
+            "frac_of_copies_only": copies_ms / (t_max * 1e3 / steps),
             "path": "pinned host -> device copies, libmsda call, device -> pinned host "
                     "copies; uploads, compute and downloads on three streams with "
                     "double-buffered device buffers (step i+1 uploads while step i runs)"}
