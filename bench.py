@@ -442,6 +442,26 @@ def make_step(msda, w, inp, bufs, stream, ordered=None, prune=0.0, fused=False):
     runs only the ordered forward.  With `prune` > 0 it runs the pruned forward (samples
     with |A| < prune skipped)."""
     shapes, starts = inp["spatial_shapes"], inp["level_start_index"]
+    if ordered and w.backward:
+        # the ordered backward; the order as for the forward (once per input set, or in
+        # each step)
+        fn = msda.msda2d_backward_ordered if w.ndim == 2 else msda.msda3d_backward_ordered
+        if ordered == "once":
+            with __import__("torch").cuda.stream(stream):
+                for b in bufs:
+                    msda.msda_query_order(b["loc"], query_order=b["order"], workspace=b["ws"],
+                                          stream=stream)
+
+        def step(i):
+            b = bufs[i % len(bufs)]
+            if ordered != "once":
+                msda.msda_query_order(b["loc"], query_order=b["order"], workspace=b["ws"],
+                                      stream=stream)
+            fn(b["value"], shapes, starts, b["loc"], b["attn"], b["order"], b["grad_out"],
+               grad_value=b["gv"], grad_sampling_locations=b["gl"],
+               grad_attention_weights=b["ga"], stream=stream)
+        # zero-fill and backward (+ keys, scan, scatter of the order in each step)
+        return step, 2 if ordered == "once" else 5
     if fused and w.backward:
         fn = msda.msda2d_backward_fused if w.ndim == 2 else msda.msda3d_backward_fused
 
@@ -744,7 +764,10 @@ def run_ours(args):
                                 "fused-prologue msda fwd" if args.fused else "msda fwd")
                                if not w.backward else
                                ("zero-fill + fused-prologue msda bwd + epilogues" if args.fused
-                                else "zero-fill + msda bwd")},
+                                else "query order + zero-fill + ordered msda bwd"
+                                if args.order == "step" else
+                                "zero-fill + ordered msda bwd (order computed once per input "
+                                "set)" if args.order == "once" else "zero-fill + msda bwd")},
         "warm_l2": {"ms_per_step": t_warm * 1e3 / n_warm,
                     "value": w.samples * n_warm / t_warm, "unit": UNIT, "steps": n_warm,
                     "note": "rank 0; one input set back to back, outside the timed region"},
@@ -881,9 +904,10 @@ def run_config(w: workloads.Workload, args, world: int) -> dict:
     treats L2.  Both arms print the same dict for the same command-line flags."""
     return {**workload_config(w),
             "query_order": {"step": "computed each step (msda_query_order) and used by the "
-                                    "ordered forward",
+                                    f"ordered {'backward' if w.backward else 'forward'}",
                             "once": "computed once per input set before the timed region "
-                                    "(msda_query_order); each step runs the ordered forward",
+                                    "(msda_query_order); each step runs the ordered "
+                                    f"{'backward' if w.backward else 'forward'}",
                             None: "as given"}[args.order],
             "prologue": ("fused: reference points + pixel offsets + logits in, "
                          "softmax and locations in the kernel") if args.fused
@@ -1079,11 +1103,12 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--workload", choices=workloads.names(), default="encoder2d")
     ap.add_argument("--order", nargs="?", const="step", default=None,
                     choices=["step", "once"],
-                    help="forward workloads: run the ordered forward with the locality-aware "
-                         "query order computed inside each step ('step', the default), or "
-                         "computed once per input set before the timed region ('once': an "
-                         "encoder's layers share their reference points and can share one "
-                         "order)")
+                    help="run the ordered forward (backward workloads: the ordered backward) "
+                         "with the locality-aware query order computed inside each step "
+                         "('step', the default), or computed once per input set before the "
+                         "timed region ('once': an encoder's layers share their reference "
+                         "points and can share one order, and a backward can reuse its "
+                         "forward's order)")
     ap.add_argument("--fused", action="store_true",
                     help="reference points, pixel offsets and logits in; the kernel forms "
                          "locations and the softmax (backward workloads: the fused backward, "
@@ -1112,8 +1137,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if (args.order or args.prune > 0) and workloads.WORKLOADS[args.workload].backward:
-        ap.error("--order and --prune apply to the forward workloads")
+    if args.prune > 0 and workloads.WORKLOADS[args.workload].backward:
+        ap.error("--prune applies to the forward workloads")
     if sum([bool(args.order), args.prune > 0, bool(args.fused)]) > 1:
         ap.error("--order, --prune and --fused are separate modes")
     if args.fused:

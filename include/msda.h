@@ -252,6 +252,19 @@ msda_status msda3d_forward_pruned(const msda_dims *dims, const void *value,
  * aligned, device memory).  Entries outside [0, Nq) are clamped into range, which gives
  * wrong results for the affected queries but never an out-of-range access; a query that
  * appears twice is computed twice and one that is missing is not written.
+ *
+ * msda2d_backward_ordered / msda3d_backward_ordered compute what msda2d_backward /
+ * msda3d_backward compute, walking the queries of batch b in the order
+ * query_order[b][0 .. Nq-1] (same requirements as for the ordered forward).  The location
+ * and weight gradients of every sample are bit for bit those of the plain call; grad_value
+ * equals it up to the order of the fp32 reductions, which is unspecified in both.  With
+ * a locality order the work in flight covers a compact region of the maps for all heads
+ * at once, which keeps the reductions' working set in L2: on a B300, the volume backward
+ * (randomly placed queries) took 694 us per step against 725 us for the plain call.
+ * Queries that already come in a local order (raster order, as in an encoder) do better
+ * with the plain call (397 us against 429 us on the encoder backward).  A query that appears
+ * twice adds its grad_value contribution twice; one that is missing gets no location or
+ * weight gradient written and adds nothing.
  */
 msda_status msda_query_order_workspace_size(const msda_dims *dims, int32_t ndim, size_t *bytes);
 
@@ -287,6 +300,24 @@ msda_status msda3d_forward_ordered(const msda_dims *dims, const void *value,
                                    const int64_t *spatial_shapes, const int64_t *level_start_index,
                                    const float *sampling_locations, const float *attention_weights,
                                    const int32_t *query_order, void *out, msda_stream_t stream);
+
+msda_status msda2d_backward_ordered(const msda_dims *dims, const void *value,
+                                    const int64_t *spatial_shapes,
+                                    const int64_t *level_start_index,
+                                    const float *sampling_locations,
+                                    const float *attention_weights, const int32_t *query_order,
+                                    const void *grad_out, float *grad_value,
+                                    float *grad_sampling_locations,
+                                    float *grad_attention_weights, msda_stream_t stream);
+
+msda_status msda3d_backward_ordered(const msda_dims *dims, const void *value,
+                                    const int64_t *spatial_shapes,
+                                    const int64_t *level_start_index,
+                                    const float *sampling_locations,
+                                    const float *attention_weights, const int32_t *query_order,
+                                    const void *grad_out, float *grad_value,
+                                    float *grad_sampling_locations,
+                                    float *grad_attention_weights, msda_stream_t stream);
 
 /* Message for the last non-OK status returned on this thread ("" if none).  The string
  * is owned by the library and stays valid until the next call on the same thread. */

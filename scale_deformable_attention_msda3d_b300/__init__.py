@@ -5,7 +5,7 @@ The compute path is libmsda.so (hand-written sm_103a CUDA kernels behind the C A
 
     msda2d_forward, msda2d_backward, msda3d_forward, msda3d_backward,
     msda_query_order, msda2d_forward_ordered, msda3d_forward_ordered,
-    msda2d_forward_pruned, msda3d_forward_pruned, msda2d_forward_fused, msda3d_forward_fused,
+    msda2d_backward_ordered, msda3d_backward_ordered, msda2d_forward_pruned, msda3d_forward_pruned, msda2d_forward_fused, msda3d_forward_fused,
     msda2d_backward_fused, msda3d_backward_fused, msda_last_error, msda_abi_version,
     msda_build_flags, msda_debug_bounds_status, msda_debug_bounds_selftest
 
@@ -19,7 +19,8 @@ build writes ``libmsda_debug.so``, which checks every corner row index before it
 from ._binding import (EXPORTS, MSDA_BF16, MSDA_ERR_CUDA, MSDA_ERR_INTERNAL,  # noqa: F401
                        MSDA_ERR_INVALID_ARG, MSDA_ERR_UNSUPPORTED, MSDA_F32, MSDA_MAX_LEVELS,
                        MSDA_MAX_POINTS, MSDA_OK, MSDA_BUILD_DEBUG_BOUNDS, MsdaError,
-                       backward_raw, forward_ordered_raw, msda_build_flags,
+                       backward_raw, backward_ordered_raw, forward_ordered_raw,
+                       msda2d_backward_ordered, msda3d_backward_ordered, msda_build_flags,
                        msda_debug_bounds_status, msda_debug_bounds_selftest,
                        forward_pruned_raw, msda2d_forward_pruned, msda3d_forward_pruned,
                        forward_fused_raw, msda2d_forward_fused, msda3d_forward_fused,

@@ -29,7 +29,7 @@ EXPORTS = ("msda2d_forward", "msda2d_backward", "msda3d_forward", "msda3d_backwa
            "msda_query_order_static", "msda2d_forward_pruned", "msda3d_forward_pruned",
            "msda2d_forward_fused", "msda3d_forward_fused", "msda2d_backward_fused",
            "msda3d_backward_fused", "msda_build_flags", "msda_debug_bounds_status",
-           "msda_debug_bounds_selftest")
+           "msda_debug_bounds_selftest", "msda2d_backward_ordered", "msda3d_backward_ordered")
 MSDA_BUILD_DEBUG_BOUNDS = 1
 
 
@@ -86,6 +86,10 @@ def load(path: Optional[str] = None):
         fwd_o = [_DIMS_P, _VP, _I64P, _I64P, _VP, _VP, _VP, _VP, _VP]
         for name in ("msda2d_forward_ordered", "msda3d_forward_ordered"):
             getattr(lib, name).argtypes = fwd_o
+            getattr(lib, name).restype = ctypes.c_int
+        bwd_o = [_DIMS_P, _VP, _I64P, _I64P, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
+        for name in ("msda2d_backward_ordered", "msda3d_backward_ordered"):
+            getattr(lib, name).argtypes = bwd_o
             getattr(lib, name).restype = ctypes.c_int
         lib.msda_query_order_workspace_size.argtypes = [_DIMS_P, ctypes.c_int32,
                                                         ctypes.POINTER(ctypes.c_size_t)]
@@ -230,6 +234,21 @@ def backward_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes, level_s
               _VP(grad_attention_weights), _VP(stream))
 
 
+def backward_ordered_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes,
+                         level_start_index, sampling_locations: int, attention_weights: int,
+                         query_order: int, grad_out: int, grad_value: int,
+                         grad_sampling_locations: int, grad_attention_weights: int,
+                         stream: int = 0, lib=None) -> int:
+    """Call msda{2,3}d_backward_ordered with raw device pointers; returns the status."""
+    lib = lib or load()
+    sh, ls = _host_i64(spatial_shapes), _host_i64(level_start_index)
+    fn = lib.msda2d_backward_ordered if ndim == 2 else lib.msda3d_backward_ordered
+    return fn(ctypes.byref(dims), _VP(value), sh.ctypes.data_as(_I64P),
+              ls.ctypes.data_as(_I64P), _VP(sampling_locations), _VP(attention_weights),
+              _VP(query_order), _VP(grad_out), _VP(grad_value), _VP(grad_sampling_locations),
+              _VP(grad_attention_weights), _VP(stream))
+
+
 def backward_fused_raw(ndim: int, dims: msda_dims, value: int, spatial_shapes,
                        level_start_index, reference_points: int, sampling_offsets: int,
                        attention_logits: int, grad_out: int, grad_value: int,
@@ -325,7 +344,7 @@ def _forward(ndim, value, spatial_shapes, level_start_index, sampling_locations,
 
 def _backward(ndim, value, spatial_shapes, level_start_index, sampling_locations,
               attention_weights, grad_out, grad_value=None, grad_sampling_locations=None,
-              grad_attention_weights=None, stream=None):
+              grad_attention_weights=None, stream=None, query_order=None):
     torch = _torch()
     dims = _dims_from(value, sampling_locations, ndim)
     _require(value, "value")
@@ -345,11 +364,23 @@ def _backward(ndim, value, spatial_shapes, level_start_index, sampling_locations
     _require(grad_sampling_locations, "grad_sampling_locations", torch.float32)
     _require(grad_attention_weights, "grad_attention_weights", torch.float32)
     lib = load()
-    st = backward_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
-                      sampling_locations.data_ptr(), attention_weights.data_ptr(),
-                      grad_out.data_ptr(), grad_value.data_ptr(),
-                      grad_sampling_locations.data_ptr(), grad_attention_weights.data_ptr(),
-                      _stream_handle(stream, dev), lib=lib)
+    if query_order is None:
+        st = backward_raw(ndim, dims, value.data_ptr(), spatial_shapes, level_start_index,
+                          sampling_locations.data_ptr(), attention_weights.data_ptr(),
+                          grad_out.data_ptr(), grad_value.data_ptr(),
+                          grad_sampling_locations.data_ptr(), grad_attention_weights.data_ptr(),
+                          _stream_handle(stream, dev), lib=lib)
+    else:
+        _require(query_order, "query_order", torch.int32)
+        if tuple(query_order.shape) != (dims.B, dims.Nq):
+            raise MsdaError(MSDA_ERR_INVALID_ARG, "query_order must be [B, Nq]")
+        st = backward_ordered_raw(ndim, dims, value.data_ptr(), spatial_shapes,
+                                  level_start_index, sampling_locations.data_ptr(),
+                                  attention_weights.data_ptr(), query_order.data_ptr(),
+                                  grad_out.data_ptr(), grad_value.data_ptr(),
+                                  grad_sampling_locations.data_ptr(),
+                                  grad_attention_weights.data_ptr(),
+                                  _stream_handle(stream, dev), lib=lib)
     _check(lib, st)
     return grad_value, grad_sampling_locations, grad_attention_weights
 
@@ -387,6 +418,26 @@ def msda3d_backward(value, spatial_shapes, level_start_index, sampling_locations
     return _backward(3, value, spatial_shapes, level_start_index, sampling_locations,
                      attention_weights, grad_out, grad_value, grad_sampling_locations,
                      grad_attention_weights, stream)
+
+
+def msda2d_backward_ordered(value, spatial_shapes, level_start_index, sampling_locations,
+                            attention_weights, query_order, grad_out, grad_value=None,
+                            grad_sampling_locations=None, grad_attention_weights=None,
+                            stream=None):
+    """msda2d_backward walking each batch's queries in ``query_order`` (int32 [B, Nq])."""
+    return _backward(2, value, spatial_shapes, level_start_index, sampling_locations,
+                     attention_weights, grad_out, grad_value, grad_sampling_locations,
+                     grad_attention_weights, stream, query_order)
+
+
+def msda3d_backward_ordered(value, spatial_shapes, level_start_index, sampling_locations,
+                            attention_weights, query_order, grad_out, grad_value=None,
+                            grad_sampling_locations=None, grad_attention_weights=None,
+                            stream=None):
+    """msda3d_backward walking each batch's queries in ``query_order`` (int32 [B, Nq])."""
+    return _backward(3, value, spatial_shapes, level_start_index, sampling_locations,
+                     attention_weights, grad_out, grad_value, grad_sampling_locations,
+                     grad_attention_weights, stream, query_order)
 
 
 def msda_query_order(sampling_locations, query_order=None, workspace=None, stream=None):

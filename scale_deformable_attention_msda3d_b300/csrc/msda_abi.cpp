@@ -189,7 +189,8 @@ msda_status backward_impl(int ndim, const msda_dims *dims, const void *value,
                           const float *attn, const void *grad_out, float *grad_value,
                           float *grad_loc, float *grad_attn, msda_stream_t stream,
                           const float *ref = nullptr, float *grad_ref = nullptr,
-                          bool fused = false) {
+                          bool fused = false, const int32_t *order = nullptr,
+                          bool ordered = false) {
     msda::Params p;
     int G = 0;
     MSDA_TRY(build_params(dims, ndim, shapes, level_start, &p, &G));
@@ -207,6 +208,14 @@ msda_status backward_impl(int ndim, const msda_dims *dims, const void *value,
             MSDA_TRY(check_ptr(ref, "reference_points"));
             if (grad_ref) MSDA_TRY(check_ptr(grad_ref, "grad_reference_points"));
         }
+        if (ordered) {
+            if (!order) return fail(MSDA_ERR_INVALID_ARG, "query_order is NULL");
+            if ((reinterpret_cast<uintptr_t>(order) & 3u) != 0)
+                return fail(MSDA_ERR_INVALID_ARG, "query_order is not 4-byte aligned");
+            if (dims->Nq > INT32_MAX)
+                return fail(MSDA_ERR_UNSUPPORTED, "Nq = %lld: a query order needs Nq < 2^31",
+                            (long long)dims->Nq);
+        }
     }
     MSDA_TRY(cuda_status(msda::launch_zero_fill(grad_value, p.B * p.Nin * p.M * p.D, s),
                          "grad_value zero-fill launch"));
@@ -219,6 +228,7 @@ msda_status backward_impl(int ndim, const msda_dims *dims, const void *value,
     p.grad_attn = grad_attn;
     p.ref = fused ? ref : nullptr;
     p.grad_ref = fused ? grad_ref : nullptr;
+    p.order = ordered ? order : nullptr;
 #ifdef MSDA_DEBUG_BOUNDS
     MSDA_TRY(cuda_status(msda::debug_record(&p.dbg), "bounds-check record"));
 #endif
@@ -410,6 +420,34 @@ msda_status msda3d_backward(const msda_dims *dims, const void *value,
                          grad_attention_weights, stream);
 }
 
+msda_status msda2d_backward_ordered(const msda_dims *dims, const void *value,
+                                    const int64_t *spatial_shapes,
+                                    const int64_t *level_start_index,
+                                    const float *sampling_locations,
+                                    const float *attention_weights, const int32_t *query_order,
+                                    const void *grad_out, float *grad_value,
+                                    float *grad_sampling_locations,
+                                    float *grad_attention_weights, msda_stream_t stream) {
+    return backward_impl(2, dims, value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_weights, grad_out, grad_value, grad_sampling_locations,
+                         grad_attention_weights, stream, nullptr, nullptr, false, query_order,
+                         true);
+}
+
+msda_status msda3d_backward_ordered(const msda_dims *dims, const void *value,
+                                    const int64_t *spatial_shapes,
+                                    const int64_t *level_start_index,
+                                    const float *sampling_locations,
+                                    const float *attention_weights, const int32_t *query_order,
+                                    const void *grad_out, float *grad_value,
+                                    float *grad_sampling_locations,
+                                    float *grad_attention_weights, msda_stream_t stream) {
+    return backward_impl(3, dims, value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_weights, grad_out, grad_value, grad_sampling_locations,
+                         grad_attention_weights, stream, nullptr, nullptr, false, query_order,
+                         true);
+}
+
 msda_status msda2d_backward_fused(const msda_dims *dims, const void *value,
                                   const int64_t *spatial_shapes, const int64_t *level_start_index,
                                   const float *reference_points, const float *sampling_offsets,
@@ -485,6 +523,6 @@ msda_status msda_debug_bounds_selftest(msda_stream_t stream) {
 
 const char *msda_last_error(void) { return g_err; }
 
-int32_t msda_abi_version(void) { return 10200; }
+int32_t msda_abi_version(void) { return 10300; }
 
 }  // extern "C"

@@ -95,9 +95,10 @@ bwd2d_generic(const __grid_constant__ Params p) {
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     // whole warps leave together so that the group shuffles below see every lane
     if ((t - (threadIdx.x & 31)) / G >= p.n_items) return;
-    long long item = t / G;
-    const bool active = item < p.n_items;
-    if (!active) item = p.n_items - 1;  // tail lanes recompute a real item, write nothing
+    long long pos = t / G;
+    const bool active = pos < p.n_items;
+    if (!active) pos = p.n_items - 1;  // tail lanes recompute a real item, write nothing
+    const long long item = ordered_item(p, pos);  // the item itself without a query order
     const int sub = threadIdx.x & (G - 1);
     const int m = static_cast<int>(item % p.M);
     const long long b = item / p.M / p.Nq;
@@ -189,9 +190,10 @@ bwd3d_generic(const __grid_constant__ Params p) {
     const int P = PP > 0 ? PP : p.P;
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if ((t - (threadIdx.x & 31)) / G >= p.n_items) return;
-    long long item = t / G;
-    const bool active = item < p.n_items;
-    if (!active) item = p.n_items - 1;
+    long long pos = t / G;
+    const bool active = pos < p.n_items;
+    if (!active) pos = p.n_items - 1;
+    const long long item = ordered_item(p, pos);
     const int sub = threadIdx.x & (G - 1);
     const int m = static_cast<int>(item % p.M);
     const long long b = item / p.M / p.Nq;
@@ -319,9 +321,26 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
     constexpr int GPB = BT / G;          // lane groups (queries in flight) per CTA
 
     const int cta = blockIdx.x;
-    const int bm = cta / p.nchunk, chunk = cta - bm * p.nchunk;
-    const int m = bm % p.M;
-    const long long b = bm / p.M;
+    // CTA -> (batch, head, run of query positions).  Queries in the given order go
+    // head-major: the CTAs in flight then cover one head, whose grad_value slice and value
+    // lines stay in L2 whatever the queries' positions.  With a query order (locality
+    // sorted) the head index runs fastest instead: the CTAs in flight cover a compact
+    // region of the maps for all heads at once.  Measured on the volume backward (random
+    // voxel queries, inputs permuted on the host): head-major 738 us given, 712 us with
+    // the queries sorted; head-fastest 877 us given, 695 us sorted.
+    int m, chunk;
+    long long b;
+    if (p.order == nullptr) {
+        const int bm = cta / p.nchunk;
+        chunk = cta - bm * p.nchunk;
+        m = bm % p.M;
+        b = bm / p.M;
+    } else {
+        m = cta % p.M;
+        const int rest = cta / p.M;
+        chunk = rest % p.nchunk;
+        b = rest / p.nchunk;
+    }
     const long long q_lo = static_cast<long long>(chunk) * p.qchunk;
     const long long q_hi = q_lo + p.qchunk < p.Nq ? q_lo + p.qchunk : p.Nq;
     const int sub = threadIdx.x & (G - 1);
@@ -345,9 +364,15 @@ __device__ __forceinline__ void bwd_tiled_body(const Params &p) {
 
     {
         // one lane group per query: the launch makes a CTA's query run exactly GPB long
-        long long q = q_lo + grp;
+        long long q = q_lo + grp;   // position among the batch's queries
         const bool active = q < q_hi;
         if (!active) q = q_hi - 1;  // recompute a real query, write nothing
+        if (p.order != nullptr) {
+            // query order: position q runs query order[b * Nq + q], clamped into [0, Nq)
+            // (a malformed order gives wrong results, never an out-of-range access)
+            const int o = __ldg(p.order + b * p.Nq + q);
+            q = o < 0 ? 0 : (o >= p.Nq ? p.Nq - 1 : o);
+        }
         const long long item = (b * p.Nq + q) * p.M + m;
         const char *go_row = static_cast<const char *>(p.grad_out) + item * (rb / p.M);
         float g[N], gr[N];

@@ -36,7 +36,7 @@ struct Params {
     float *grad_value;          // [B, Nin, M, D]         (backward)
     float *grad_loc;            // like loc               (backward)
     float *grad_attn;           // like attn              (backward)
-    const int *order;           // [B, Nq] query order, or null (forward)
+    const int *order;           // [B, Nq] query order, or null (forward and backward)
     float prune;                // forward: samples with |A| < prune are skipped (0: exact)
     // fused prologue (forward): when set, `loc` holds sampling offsets in pixels of the
     // sampled level and `attn` the attention logits; the location is ref[b, q, l] + offset /

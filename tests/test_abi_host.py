@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert msda.msda_abi_version() == 10200
+    assert msda.msda_abi_version() == 10300
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -213,6 +213,20 @@ def test_ordered_forward_rejects_bad_order(lib):
     assert msda.forward_ordered_raw(2, dims(Nq=0), 0, SH2, LS2, 0, 0, 0, 0, 0) == msda.MSDA_OK
 
 
+def test_ordered_backward_rejects_bad_order(lib):
+    for order, msg in ((0, "query_order is NULL"), (FAKE + 1, "4-byte aligned")):
+        st = msda.backward_ordered_raw(2, dims(), FAKE, SH2, LS2, FAKE, FAKE, order, FAKE, FAKE,
+                                       FAKE, FAKE, 0)
+        assert st == msda.MSDA_ERR_INVALID_ARG and msg in msda.msda_last_error()
+    # the core's own checks still run first
+    st = msda.backward_ordered_raw(2, dims(M=0), FAKE, SH2, LS2, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                   FAKE, FAKE, 0)
+    assert st == msda.MSDA_ERR_INVALID_ARG
+    # an empty batch: OK without touching the device
+    assert msda.backward_ordered_raw(2, dims(B=0), 0, SH2, LS2, 0, 0, 0, 0, 0, 0, 0,
+                                     0) == msda.MSDA_OK
+
+
 @pytest.mark.parametrize("tau", [-0.1, float("nan"), float("inf")])
 def test_pruned_forward_rejects_bad_threshold(lib, tau):
     st = msda.forward_pruned_raw(2, dims(), FAKE, SH2, LS2, FAKE, FAKE, tau, FAKE, 0)
@@ -305,6 +319,8 @@ for nd in (2, 3):
             "forward_pruned": lambda: msda.forward_pruned_raw(nd, d, F, sh, ls, F, F, 0.01, F, 0),
             "forward_ordered": lambda: msda.forward_ordered_raw(nd, d, F, sh, ls, F, F, F, F, 0),
             "backward": lambda: msda.backward_raw(nd, d, F, sh, ls, F, F, F, F, F, F, 0),
+            "backward_ordered": lambda: msda.backward_ordered_raw(nd, d, F, sh, ls, F, F, F, F, F,
+                                                                  F, F, 0),
             "backward_fused": lambda: msda.backward_fused_raw(nd, d, F, sh, ls, F, F, F, F, F, F,
                                                               F, F, 0),
             "query_order": lambda: msda.query_order_raw(nd, d, F, F, F, 1 << 24, 0),
@@ -328,7 +344,7 @@ def test_cuda_errors_map_to_msda_err_cuda_without_a_device():
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     res = json.loads(r.stdout.strip().splitlines()[-1])
-    assert len(res) == 2 * 2 * 8
+    assert len(res) == 2 * 2 * 9
     for key, (st, msg) in res.items():
         assert st == msda.MSDA_ERR_CUDA, (key, st, msg)
         # "<what>: <cudaError name> (<description>)"

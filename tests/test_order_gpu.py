@@ -1,16 +1,20 @@
-"""Locality-aware query order (msda_query_order, msda{2,3}d_forward_ordered) on the GPU.
+"""Locality-aware query order (msda_query_order, msda{2,3}d_forward_ordered,
+msda{2,3}d_backward_ordered) on the GPU.
 
 The order is a schedule, not part of the method's arithmetic: the ordered forward must
 give exactly the unordered forward's result (bit for bit, every item's arithmetic is the
 same), the order must be a permutation of each batch's queries, and it must actually
-bring queries with nearby samples together.
+bring queries with nearby samples together.  The ordered backward gives the plain
+backward's location and weight gradients bit for bit (each query's lane group does the
+same arithmetic) and its grad_value up to the order of the fp32 reductions.
 """
 import numpy as np
 import pytest
 
 import oracle
 import workloads
-from gpu_parity import check, device_inputs, host, run_forward
+from gpu_parity import (check, device_inputs, grad_value_magnitude, host, run_backward,
+                         run_forward)
 
 pytestmark = pytest.mark.gpu
 
@@ -130,3 +134,58 @@ def test_out_of_range_order_entries_are_clamped(msda):
     # only queries 0 and Nq-1 were computed; every other row is untouched
     check(got[:, [0, 39]], ref[:, [0, 39]], "f32", "clamped order")
     assert np.all(got[:, 1:39] == 123.0)
+
+
+# ------------------------------------------------------------------ ordered backward
+
+
+def _backward_ordered(msda, nd, d, order):
+    import torch
+    fn = msda.msda2d_backward_ordered if nd == 2 else msda.msda3d_backward_ordered
+    res = fn(d["value"], d["spatial_shapes"], d["level_start_index"], d["sampling_locations"],
+             d["attention_weights"], order, d["grad_out"])
+    torch.cuda.synchronize()
+    return res
+
+
+def _check_ordered_backward(msda, nd, inp, dtype, what, order=None):
+    d = device_inputs(inp, dtype)
+    if order is None:
+        order = _order(msda, d)
+    gv, gl, ga = _backward_ordered(msda, nd, d, order)
+    _, pgl, pga = run_backward(msda, nd, d)
+    assert np.array_equal(host(gl), host(pgl)), what
+    assert np.array_equal(host(ga), host(pga)), what
+    rgv, rgl, rga = oracle.run_inputs(nd, inp, backward_pass=True)
+    check(host(gv), rgv, "f32", what + " grad_value", grad_value_magnitude(nd, inp))
+    check(host(gl), rgl, "f32", what + " grad_sampling_locations")
+    check(host(ga), rga, "f32", what + " grad_attention_weights")
+
+
+@pytest.mark.parametrize("nd,shapes,dtype,D,P", [
+    (2, [(13, 17), (7, 5), (3, 4), (1, 2)], "f32", 32, 4),              # tiled (4, 4)
+    (2, [(13, 17), (7, 5), (3, 4)], "bf16", 16, 5),                     # generic (3, 5)
+    (3, [(5, 6, 7), (3, 2, 4), (1, 3, 2), (2, 2, 2)], "bf16", 32, 4),   # tiled, 3D
+    (3, [(5, 6, 7)], "f32", 16, 4),                                     # tiled (1, 4), 3D
+    (3, [(5, 6, 7), (3, 2, 4)], "f32", 8, 3),                           # generic 3D
+])
+def test_ordered_backward_matches_plain_and_oracle(msda, nd, shapes, dtype, D, P):
+    inp = workloads.random_problem(nd, shapes, B=3, Nq=211, M=4, D=D, P=P, dtype=dtype,
+                                   seed=100 + len(shapes) * 10 + nd * 3 + P)
+    _check_ordered_backward(msda, nd, inp, dtype, f"ordered backward {nd}d {dtype} L{len(shapes)}")
+
+
+def test_ordered_backward_reversed_order(msda):
+    import torch
+    inp = workloads.random_problem(2, [(9, 11), (4, 6), (2, 3), (1, 2)], B=2, Nq=77, M=2,
+                                   D=32, P=4, seed=33)
+    rev = torch.arange(76, -1, -1, dtype=torch.int32, device="cuda").repeat(2, 1).contiguous()
+    _check_ordered_backward(msda, 2, inp, "f32", "ordered backward, reversed order", rev)
+
+
+def test_ordered_backward_volume_full_size(msda):
+    """The volume backward (bf16 value, 10 % of the samples out of range) with its queries
+    in the locality order: the configuration this entry point is for."""
+    w = workloads.WORKLOADS["volume3d_bwd"]
+    inp = workloads.make_inputs(w)
+    _check_ordered_backward(msda, 3, inp, w.dtype, "ordered volume3d_bwd")
