@@ -259,8 +259,9 @@ msda_status msda3d_forward_pruned(const msda_dims *dims, const void *value,
  * and weight gradients of every sample are bit for bit those of the plain call; grad_value
  * equals it up to the order of the fp32 reductions, which is unspecified in both.  With
  * a locality order the work in flight covers a compact region of the maps for all heads
- * at once, which keeps the reductions' working set in L2: on a B300, the volume backward
- * (randomly placed queries) took 694 us per step against 725 us for the plain call.
+ * at once, so the value lines that neighbouring heads share are fetched once: on a B300
+ * the volume backward (randomly placed queries) took 694 us per step against 725 us for
+ * the plain call.
  * Queries that already come in a local order (raster order, as in an encoder) do better
  * with the plain call (397 us against 429 us on the encoder backward).  A query that appears
  * twice adds its grad_value contribution twice; one that is missing gets no location or
