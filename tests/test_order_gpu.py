@@ -189,3 +189,30 @@ def test_ordered_backward_volume_full_size(msda):
     w = workloads.WORKLOADS["volume3d_bwd"]
     inp = workloads.make_inputs(w)
     _check_ordered_backward(msda, 3, inp, w.dtype, "ordered volume3d_bwd")
+
+
+def test_autograd_wrapper_with_a_query_order(msda):
+    """ms_deform_attn(..., query_order=...) runs the ordered forward and backward: the same
+    output bit for bit, the same location and weight gradients bit for bit, grad_value up
+    to the order of its fp32 sums."""
+    import torch
+    inp = workloads.random_problem(3, [(5, 6, 7), (3, 2, 4), (1, 3, 2), (2, 2, 2)], B=2,
+                                   Nq=150, M=8, D=32, P=4, dtype="bf16", seed=41)
+    d = device_inputs(inp, "bf16")
+    order = _order(msda, d)
+    res = []
+    for qo in (None, order):
+        v = d["value"].detach().clone().requires_grad_(True)
+        loc = d["sampling_locations"].detach().clone().requires_grad_(True)
+        a = d["attention_weights"].detach().clone().requires_grad_(True)
+        out = msda.ms_deform_attn(v, d["spatial_shapes"], d["level_start_index"], loc, a,
+                                  query_order=qo)
+        out.backward(d["grad_out"])
+        torch.cuda.synchronize()
+        res.append((host(out), host(v.grad), host(loc.grad), host(a.grad)))
+    (o0, gv0, gl0, ga0), (o1, gv1, gl1, ga1) = res
+    assert np.array_equal(o0, o1)
+    assert np.array_equal(gl0, gl1) and np.array_equal(ga0, ga1)
+    rgv, _, _ = oracle.run_inputs(3, inp, backward_pass=True)
+    # value's gradient comes back in value's dtype (bf16: the fp32 sum rounded once)
+    check(gv1, rgv, "bf16", "autograd ordered grad_value", grad_value_magnitude(3, inp))
